@@ -1,0 +1,136 @@
+"""Plants plausible mistakes in the CPU oracle and checks that a pin catches
+each one.  Every mutation is applied by monkeypatching the oracle module for
+the duration of one test; nothing here touches a GPU."""
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.lopt_oracle as L
+from tests import test_oracle_pins as pins
+
+PIN_TESTS = [
+    lambda: pins.test_p1_ema_closed_form(2),
+    lambda: pins.test_p2_factored_rank1(3),
+    lambda: pins.test_features_closed_form(4),
+    pins.test_p3_unit_mean_square,
+    lambda: pins.test_p4_normalised_sgd(0.5, 250.0, 4),
+    pins.test_p4_golden_normalised_sgd,
+    pins.test_p4_last_element_feature,
+    pins.test_p4_time_feature_not_normalised,
+    pins.test_p4_second_relu_and_biases,
+    pins.test_p6_gradient_scale_invariance,
+    pins.test_p7_indexing_tags,
+]
+
+
+def _some_pin_fails():
+    for t in PIN_TESTS:
+        try:
+            t()
+        except AssertionError:
+            return True
+    return False
+
+
+def _features_with(mutate):
+    orig = L.features
+
+    def f(*a, **k):
+        return mutate(orig(*a, **k))
+    return f
+
+
+def _mlp_no_relu(layer):
+    def mlp(X, w):
+        z1 = X @ w.W1 + w.b1
+        h1 = z1 if layer == 1 else np.maximum(z1, 0.0)
+        z2 = h1 @ w.W2 + w.b2
+        h2 = z2 if layer == 2 else np.maximum(z2, 0.0)
+        return h2 @ w.W3 + w.b3
+    return mlp
+
+
+def _unpack_transposed(flat, hidden):
+    w = _orig_unpack(flat, hidden)
+    n = L.D_FEAT * hidden
+    w.W1 = np.asarray(flat, dtype=np.float64)[:n].reshape(hidden, L.D_FEAT).T
+    return w
+
+
+_orig_unpack = L.unpack_weights
+
+
+def _swap_index_19(F):
+    F = F.copy()
+    blk = F[:, 19:28].reshape(-1, 3, 3).transpose(0, 2, 1).reshape(-1, 9)
+    F[:, 19:28] = blk
+    return F
+
+
+def _factored_sums(g2d, row, col):
+    sq = g2d * g2d
+    G, H = sq.sum(axis=1), sq.sum(axis=0)
+    nr = [b * row[k] + (1 - b) * G for k, b in enumerate(L.FACTORED_DECAYS)]
+    nc = [b * col[k] + (1 - b) * H for k, b in enumerate(L.FACTORED_DECAYS)]
+    return nr, nc, [float(r.mean()) for r in nr]
+
+
+def _vhat_swapped(r, c, rho, i, j):
+    R, C = r.size, c.size
+    e = i * C + j
+    i2, j2 = e % R, (e // R) % C
+    return r[i2] * c[j2] / rho if rho > 0 else np.zeros(i.shape)
+
+
+def _normalise_all(F, scales):
+    Fn = F.copy()
+    Fn[:, :L.N_ELEM_FEATURES] *= scales[None, :]
+    rms = np.sqrt((F[:, L.N_ELEM_FEATURES:] ** 2).mean(axis=0) + L.EPS)
+    Fn[:, L.N_ELEM_FEATURES:] /= rms[None, :]
+    return Fn
+
+
+def _scales_std(S, n):
+    return 1.0 / np.sqrt(S / float(n) * 2.0 + L.EPS)
+
+
+def _sqrt_v_dropped(F):
+    F = F.copy()
+    F[:, 5] = F[:, 5] ** 2
+    return F
+
+
+MUTATIONS = {
+    "momentum decays reversed": ("MOMENTUM_DECAYS", (0.9, 0.5, 0.1)),
+    "rms decay 0.99": ("RMS_DECAY", 0.99),
+    "factored decays reversed": ("FACTORED_DECAYS", (0.9, 0.5, 0.1)),
+    "factored sums not means": ("factored_update", _factored_sums),
+    "vhat indices transposed": ("factored_vhat", _vhat_swapped),
+    "feature 5 is v not sqrt(v)": ("features", _features_with(_sqrt_v_dropped)),
+    "m_a*rsqrt(vhat_b) index swapped": ("features", _features_with(_swap_index_19)),
+    "time features normalised": ("normalise", _normalise_all),
+    "normalised by a wrong mean square": ("normalisation_scales", _scales_std),
+    "no ReLU after layer 1": ("mlp", _mlp_no_relu(1)),
+    "no ReLU after layer 2": ("mlp", _mlp_no_relu(2)),
+    "W1 read transposed": ("unpack_weights", _unpack_transposed),
+    "update sign flipped": ("update_from_output",
+                            lambda o: -o[:, 0] * np.exp(o[:, 1] * 1e-3) * 1e-3),
+    "magnitude not scaled": ("update_from_output",
+                             lambda o: o[:, 0] * np.exp(o[:, 1]) * 1e-3),
+    "time features off by one step": ("time_features",
+                                      lambda t: np.tanh((float(t) + 1) / np.asarray(L.TIME_SCALES))),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_mutation_is_caught(name, monkeypatch):
+    attr, value = MUTATIONS[name]
+    monkeypatch.setattr(L, attr, value)
+    if hasattr(oracle, attr):
+        monkeypatch.setattr(oracle, attr, value)
+    assert _some_pin_fails(), "no pin caught: " + name
+
+
+def test_unmutated_oracle_passes_all_pins():
+    assert not _some_pin_fails()
