@@ -1,0 +1,193 @@
+/*
+ * lopt.h -- C ABI of the GB300 learned-optimizer step library (liblopt.so).
+ *
+ * One call, lopt_step(), performs one step of a small_fc_lopt-style learned
+ * optimizer over a whole list of parameter tensors on one GPU:
+ *
+ *   for every element of every tensor
+ *     - update three momenta, one RMS accumulator and the Adafactor-factored
+ *       row/column accumulators from the gradient,
+ *     - build the 39-wide feature vector (28 per-element features + 11
+ *       time features),
+ *     - divide each per-element feature by its root-mean-square over the
+ *       whole tensor,
+ *     - run the per-element MLP 39 -> H -> H -> 2 (ReLU, ReLU, linear),
+ *     - update = direction * exp(magnitude * 1e-3) * 1e-3,
+ *       param -= lr * update.
+ *
+ * Method: "PyLO: Towards Accessible Learned Optimizers in PyTorch" (MLSys 2026
+ * talk notes), sections "融合カーネル戦略" (kernel 1 = features + per-feature
+ * sum of squares, kernel 2 = features + normalisation + MLP + update),
+ * "メモリ階層の活用" (features in registers, statistics in shared memory,
+ * d_feat ~ 39, d_hidden ~ 32) and "PyLO のライブラリ設計" (per-parameter
+ * accumulators kept by the optimiser).
+ *
+ * Conventions for every entry point
+ *   - Return 0 (LOPT_OK) on success, a negative LOPT_E_* code otherwise;
+ *     lopt_strerror() names the code.
+ *   - Device pointers are CUDA global-memory addresses on the device that was
+ *     current when the handle was created; host pointers are ordinary CPU
+ *     memory.  No pointer is retained past the call that receives it, except
+ *     that lopt_step() enqueues GPU work that reads and writes the tensor
+ *     buffers until that work has completed on the given stream.
+ *   - Nothing in this ABI uses C++ or PyTorch types.
+ */
+#ifndef LOPT_H
+#define LOPT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- error codes ------------------------------------------------------- */
+#define LOPT_OK             0
+#define LOPT_E_ARG         -1  /* null / out-of-range argument            */
+#define LOPT_E_SHAPE       -2  /* rows*cols < 1 or too large               */
+#define LOPT_E_ALIGN       -3  /* a tensor pointer is not 4-byte aligned   */
+#define LOPT_E_CUDA        -4  /* a CUDA runtime call failed               */
+#define LOPT_E_OOM         -5  /* device workspace allocation failed       */
+#define LOPT_E_UNSUPPORTED -6  /* hidden width / MLP path not available    */
+#define LOPT_E_TIMEOUT     -7  /* a bounded device-side wait gave up       */
+#define LOPT_E_ALIAS       -8  /* two tensor buffers overlap               */
+
+/* ---- fixed sizes ------------------------------------------------------- */
+#define LOPT_D_FEAT        39  /* 28 per-element + 11 time features        */
+#define LOPT_N_STATS       28  /* normalised (per-element) features        */
+#define LOPT_MAX_HIDDEN    64
+
+/* ---- MLP evaluation paths (lopt_set_mlp_path) -------------------------- */
+#define LOPT_MLP_FP32       0  /* FP32 FMA on CUDA cores (default)          */
+#define LOPT_MLP_TC         1  /* tcgen05 tensor cores, TF32/FP16 operands, */
+                               /* FP32 accumulation                         */
+
+typedef struct lopt_ctx* lopt_handle;
+
+/*
+ * One parameter tensor.  All pointers are DEVICE pointers to contiguous fp32
+ * arrays, owned by the caller; lopt_step() updates them in place.
+ *
+ *   param   [rows*cols]  read, then overwritten with the stepped values
+ *   grad    [rows*cols]  read only
+ *   mom[k]  [rows*cols]  momentum with decay 0.1, 0.5, 0.9 (k = 0, 1, 2)
+ *   rms     [rows*cols]  second moment, decay 0.999
+ *   row[k]  [rows]       Adafactor row accumulator, decay 0.1, 0.5, 0.9
+ *   col[k]  [cols]       Adafactor column accumulator, decay 0.1, 0.5, 0.9
+ *
+ * Layout: element (i, j) of the [rows x cols] view sits at i*cols + j.  A
+ * rank-1 tensor of n elements is passed as rows = 1, cols = n; a rank-0
+ * tensor as 1 x 1; rank >= 3 as prod(leading dims) x last dim.
+ * Accumulators must be zero before the first step.  No buffer may overlap
+ * another buffer of the same call.
+ * weight_set selects one of the MLP weight sets given to lopt_create().
+ */
+typedef struct {
+  float*       param;
+  const float* grad;
+  float*       mom[3];
+  float*       rms;
+  float*       row[3];
+  float*       col[3];
+  int64_t      rows;
+  int64_t      cols;
+  int32_t      weight_set;
+  int32_t      reserved;   /* must be 0 */
+} lopt_tensor;
+
+/*
+ * Number of floats in one MLP weight set for the given widths:
+ * d_feat*H + H + H*H + H + 2*H + 2.
+ */
+int lopt_weight_set_size(int d_feat, int hidden);
+
+/*
+ * Create a handle on the current CUDA device.
+ *   mlp_weights  HOST pointer, n_sets consecutive weight sets, each laid out
+ *                row-major as W1[d_feat][H], b1[H], W2[H][H], b2[H],
+ *                W3[H][2], b3[2]  (h1 = ReLU(x W1 + b1), h2 = ReLU(h1 W2 + b2),
+ *                (direction, magnitude) = h2 W3 + b3).  Copied to the device;
+ *                the caller may free it after the call returns.
+ *   d_feat       must be LOPT_D_FEAT (39).
+ *   hidden       1 .. LOPT_MAX_HIDDEN.
+ *   n_sets       >= 1.
+ *   out          receives the handle.
+ * Errors: LOPT_E_ARG (bad pointer / size), LOPT_E_UNSUPPORTED (hidden out of
+ * range), LOPT_E_CUDA / LOPT_E_OOM (device failure; *out is left NULL).
+ * Synchronous.
+ */
+int lopt_create(const float* mlp_weights, int d_feat, int hidden, int n_sets,
+                lopt_handle* out);
+
+/*
+ * Choose how the MLP is evaluated by later lopt_step() calls:
+ * LOPT_MLP_FP32 (exact FP32 arithmetic) or LOPT_MLP_TC (tensor cores: TF32
+ * first layer, FP16 second and output layers, FP32 accumulation; about 1e-3
+ * relative error on the update).  LOPT_E_UNSUPPORTED if the path cannot run
+ * this handle's hidden width.
+ */
+int lopt_set_mlp_path(lopt_handle h, int path);
+
+/*
+ * One learned-optimizer step over n_tensors tensors (HOST array of
+ * descriptors; it is read during the call only).
+ *   t       1-based step count (drives the 11 time features tanh(t / x_s)).
+ *   lr      multiplies the update (param -= lr * update).
+ *   stream  cudaStream_t to enqueue on (NULL = legacy default stream).
+ * The whole list is processed by three kernel launches (row/column moments,
+ * feature statistics, normalise + MLP + apply).  Asynchronous: returns once
+ * the work is enqueued.  Validation happens before anything is enqueued and
+ * a failed validation leaves every buffer untouched.  Calls on one handle
+ * are ordered with each other even across streams; a handle must not be
+ * used from two host threads at once.
+ * Errors: LOPT_E_ARG, LOPT_E_SHAPE, LOPT_E_ALIGN, LOPT_E_ALIAS (validation);
+ * LOPT_E_OOM (workspace growth); LOPT_E_CUDA (launch failure).
+ */
+int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
+              int64_t t, float lr, void* stream);
+
+/*
+ * Wait for the handle's last step and report device-side status:
+ * LOPT_OK, LOPT_E_TIMEOUT (a bounded wait inside a kernel gave up; that
+ * step's results are invalid) or LOPT_E_CUDA.  Clears the status.
+ */
+int lopt_check(lopt_handle h);
+
+/*
+ * Per-feature sums of squares S_d (d = 0..27) that the last step computed
+ * for tensor `index` of its list: S_d = sum over elements of feature_d^2,
+ * the statistic the normalisation divides by (as sqrt(S_d / N + 1e-30)).
+ * out: HOST array of at least LOPT_N_STATS doubles.  Synchronous.
+ */
+int lopt_feature_stats(lopt_handle h, int index, double* out);
+
+/*
+ * Per-kernel device timing of later steps.  enable = 1 makes lopt_step()
+ * record CUDA events on its stream around each of its three launches
+ * (enable = 0, the default, records none).
+ */
+int lopt_set_kernel_timing(lopt_handle h, int enable);
+
+/*
+ * Device time summed over the steps timed since timing was enabled or since
+ * the last call: ms[0] row/column kernel, ms[1] statistics kernel, ms[2]
+ * apply kernel (milliseconds, CUDA-event resolution); launches[k] = number of
+ * launches summed.  ms and launches: HOST arrays of 3.  Waits for the last
+ * timed step; resets the sums.
+ */
+int lopt_kernel_times(lopt_handle h, double* ms, int64_t* launches);
+
+/* Release every device allocation of the handle (waits for its work). */
+int lopt_destroy(lopt_handle h);
+
+/* Static string naming an error code. */
+const char* lopt_strerror(int code);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int lopt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOPT_H */

@@ -1,0 +1,489 @@
+// Host side of liblopt: the C ABI declared in include/lopt.h.
+//
+// Builds the ragged schedule of a parameter list (one descriptor per tensor,
+// one unit table per kernel), keeps the device workspace, and enqueues the
+// three launches of a step:
+//   K0 rowcol  -- factored row/column second moments (all tensors)
+//   K1 stats   -- features + per-feature sum of squares, folded layer-1 weights
+//   K2 apply   -- features + normalise + MLP + update (FP32 or tensor cores)
+// The page ("PyLO: Towards Accessible Learned Optimizers in PyTorch", section
+// "メモリ階層の活用") counts 30-114 launches per step for a whole model with
+// its two fused kernels per tensor; here the whole list takes three.
+#include <algorithm>
+#include <cstddef>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "lopt.h"
+#include "lopt_internal.cuh"
+
+namespace lopt {
+bool apply_fp32_supported(int hidden);
+}
+
+using namespace lopt;
+
+struct lopt_ctx {
+  int device = 0;
+  int hidden = 0;        // caller's width
+  int hp = 0;            // padded width used by the kernels
+  int n_sets = 0;
+  int path = LOPT_MLP_FP32;
+  float* d_weights = nullptr;  // [n_sets][w_set_size(hp)], zero-padded
+  // workspace
+  char* d_ws = nullptr;
+  size_t ws_bytes = 0;
+  // carved views (valid for the cached schedule)
+  TensorDesc* d_desc = nullptr;
+  Unit* d_units[3] = {nullptr, nullptr, nullptr};
+  TensorAux* d_aux = nullptr;
+  int32_t* d_counters = nullptr;   // [2][T]
+  float* d_colpart = nullptr;
+  double* d_rowpart = nullptr;
+  float* d_k1part = nullptr;
+  float* d_w1fold = nullptr;
+  int32_t* d_status = nullptr;
+  int w1fold_stride = 0;
+  int n_units[3] = {0, 0, 0};
+  int n_tensors = 0;
+  // cached schedule key
+  std::vector<lopt_tensor> last_list;
+  int last_path = -1;
+  // ordering across calls
+  cudaEvent_t done = nullptr;
+  bool has_done = false;
+  // optional per-kernel timing: 4 events per timed step
+  bool timing = false;
+  std::vector<cudaEvent_t> tev;
+  size_t tev_used = 0;
+};
+
+namespace {
+
+int cuda_fail(cudaError_t e) {
+  if (e == cudaErrorMemoryAllocation) return LOPT_E_OOM;
+  return LOPT_E_CUDA;
+}
+
+int padded_hidden(int h) {
+  for (int c : {4, 8, 16, 32, 64})
+    if (h <= c) return c;
+  return -1;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Interval {
+  uintptr_t lo, hi;
+};
+
+int validate(const lopt_ctx* h, const lopt_tensor* ts, int n) {
+  std::vector<Interval> iv;
+  iv.reserve((size_t)n * 12);
+  for (int i = 0; i < n; ++i) {
+    const lopt_tensor& t = ts[i];
+    if (t.reserved != 0) return LOPT_E_ARG;
+    if (t.weight_set < 0 || t.weight_set >= h->n_sets) return LOPT_E_ARG;
+    if (t.rows < 1 || t.cols < 1) return LOPT_E_SHAPE;
+    if (t.rows > (int64_t)1 << 31 || t.cols > (int64_t)1 << 31) return LOPT_E_SHAPE;
+    const int64_t N = t.rows * t.cols;
+    if (N >= ((int64_t)1 << 31)) return LOPT_E_SHAPE;
+    const void* ep[6] = {t.param, t.grad, t.mom[0], t.mom[1], t.mom[2], t.rms};
+    for (const void* p : ep) {
+      if (!p) return LOPT_E_ARG;
+      if ((uintptr_t)p % 4) return LOPT_E_ALIGN;
+      iv.push_back({(uintptr_t)p, (uintptr_t)p + (uintptr_t)N * 4});
+    }
+    for (int k = 0; k < 3; ++k) {
+      if (!t.row[k] || !t.col[k]) return LOPT_E_ARG;
+      if ((uintptr_t)t.row[k] % 4 || (uintptr_t)t.col[k] % 4) return LOPT_E_ALIGN;
+      iv.push_back({(uintptr_t)t.row[k], (uintptr_t)t.row[k] + (uintptr_t)t.rows * 4});
+      iv.push_back({(uintptr_t)t.col[k], (uintptr_t)t.col[k] + (uintptr_t)t.cols * 4});
+    }
+  }
+  std::sort(iv.begin(), iv.end(), [](const Interval& a, const Interval& b) { return a.lo < b.lo; });
+  for (size_t k = 1; k < iv.size(); ++k)
+    if (iv[k].lo < iv[k - 1].hi) return LOPT_E_ALIAS;
+  return LOPT_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+// Rows per K0 strip: about kStripTarget elements, at most kMaxStrips strips,
+// at most 512 rows (the kernel's shared row buffer).
+int strip_rows_for(int64_t R, int64_t C) {
+  int64_t rows = std::max<int64_t>(1, kStripTarget / std::max<int64_t>(C, 1));
+  rows = std::max<int64_t>(rows, (R + kMaxStrips - 1) / kMaxStrips);
+  rows = std::min<int64_t>(rows, 512);
+  rows = std::min<int64_t>(rows, R);
+  return (int)std::max<int64_t>(rows, 1);
+}
+
+int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t stream) {
+  std::vector<TensorDesc> desc(n);
+  std::vector<Unit> units[3];
+  int64_t colpart = 0, rowpart = 0, k1part = 0;
+  for (int i = 0; i < n; ++i) {
+    const lopt_tensor& t = ts[i];
+    TensorDesc& d = desc[i];
+    std::memset(&d, 0, sizeof(d));
+    d.p = t.param;
+    d.g = t.grad;
+    for (int k = 0; k < 3; ++k) {
+      d.m[k] = t.mom[k];
+      d.r[k] = t.row[k];
+      d.c[k] = t.col[k];
+    }
+    d.v = t.rms;
+    d.R = t.rows;
+    d.C = t.cols;
+    d.N = t.rows * t.cols;
+    d.wset = t.weight_set;
+    bool v4 = aligned16(t.param) && aligned16(t.grad) && aligned16(t.rms);
+    for (int k = 0; k < 3; ++k) v4 = v4 && aligned16(t.mom[k]) && aligned16(t.col[k]);
+    d.vec4 = v4 ? 1 : 0;
+    d.strip_rows = strip_rows_for(d.R, d.C);
+    d.n_strips = (int)((d.R + d.strip_rows - 1) / d.strip_rows);
+    d.k1_units = (int)((d.N + kStatsChunk - 1) / kStatsChunk);
+    d.k2_units = (int)((d.N + kApplyChunk - 1) / kApplyChunk);
+    d.colpart_off = colpart;
+    colpart += (int64_t)d.n_strips * d.C;
+    d.rowpart_off = (int32_t)rowpart;
+    rowpart += 3 * (int64_t)d.n_strips;
+    d.k1_part_off = (int32_t)k1part;
+    k1part += (int64_t)kStats * d.k1_units;
+    if (rowpart > INT32_MAX || k1part > INT32_MAX) return LOPT_E_SHAPE;
+    for (int s = 0; s < d.n_strips; ++s) units[0].push_back({i, s});
+    for (int s = 0; s < d.k1_units; ++s) units[1].push_back({i, s});
+    for (int s = 0; s < d.k2_units; ++s) units[2].push_back({i, s});
+  }
+  h->w1fold_stride = w1fold_floats(h->hp, h->path);
+
+  // carve the workspace
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_desc = take(sizeof(TensorDesc) * n);
+  size_t o_units[3];
+  for (int k = 0; k < 3; ++k) o_units[k] = take(sizeof(Unit) * units[k].size());
+  const size_t o_aux = take(sizeof(TensorAux) * n);
+  const size_t o_cnt = take(sizeof(int32_t) * 2 * n);
+  const size_t o_col = take(sizeof(float) * colpart);
+  const size_t o_row = take(sizeof(double) * rowpart);
+  const size_t o_k1 = take(sizeof(float) * k1part);
+  const size_t o_w1 = take(sizeof(float) * (size_t)h->w1fold_stride * n);
+  const size_t o_st = take(sizeof(int32_t) * 4);
+  const size_t need = off;
+
+  if (need > h->ws_bytes) {
+    // the previous step may still be reading the old workspace
+    if (h->has_done) cudaEventSynchronize(h->done);
+    if (h->d_ws) cudaFree(h->d_ws);
+    h->d_ws = nullptr;
+    h->ws_bytes = 0;
+    cudaError_t e = cudaMalloc(&h->d_ws, need);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      h->d_ws = nullptr;
+      h->last_list.clear();
+      return LOPT_E_OOM;
+    }
+    h->ws_bytes = need;
+    e = cudaMemsetAsync(h->d_ws, 0, need, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  } else {
+    // counters and status must start at zero for a new layout
+    cudaError_t e = cudaMemsetAsync(h->d_ws + o_cnt, 0, sizeof(int32_t) * 2 * n, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaMemsetAsync(h->d_ws + o_st, 0, sizeof(int32_t) * 4, stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  h->d_desc = reinterpret_cast<TensorDesc*>(h->d_ws + o_desc);
+  for (int k = 0; k < 3; ++k) h->d_units[k] = reinterpret_cast<Unit*>(h->d_ws + o_units[k]);
+  h->d_aux = reinterpret_cast<TensorAux*>(h->d_ws + o_aux);
+  h->d_counters = reinterpret_cast<int32_t*>(h->d_ws + o_cnt);
+  h->d_colpart = reinterpret_cast<float*>(h->d_ws + o_col);
+  h->d_rowpart = reinterpret_cast<double*>(h->d_ws + o_row);
+  h->d_k1part = reinterpret_cast<float*>(h->d_ws + o_k1);
+  h->d_w1fold = reinterpret_cast<float*>(h->d_ws + o_w1);
+  h->d_status = reinterpret_cast<int32_t*>(h->d_ws + o_st);
+
+  // Pageable host sources: the runtime stages them before returning, so the
+  // vectors may die right after the calls.
+  cudaError_t e = cudaMemcpyAsync(h->d_desc, desc.data(), sizeof(TensorDesc) * n,
+                                  cudaMemcpyHostToDevice, stream);
+  for (int k = 0; k < 3 && e == cudaSuccess; ++k) {
+    if (!units[k].empty())
+      e = cudaMemcpyAsync(h->d_units[k], units[k].data(), sizeof(Unit) * units[k].size(),
+                          cudaMemcpyHostToDevice, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (int k = 0; k < 3; ++k) h->n_units[k] = (int)units[k].size();
+  h->n_tensors = n;
+  h->last_list.assign(ts, ts + n);
+  h->last_path = h->path;
+  return LOPT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int lopt_version(void) { return 100; }
+
+const char* lopt_strerror(int code) {
+  switch (code) {
+    case LOPT_OK: return "ok";
+    case LOPT_E_ARG: return "invalid argument";
+    case LOPT_E_SHAPE: return "invalid tensor shape";
+    case LOPT_E_ALIGN: return "misaligned tensor pointer";
+    case LOPT_E_CUDA: return "CUDA runtime error";
+    case LOPT_E_OOM: return "device allocation failed";
+    case LOPT_E_UNSUPPORTED: return "unsupported configuration";
+    case LOPT_E_TIMEOUT: return "device-side wait timed out";
+    case LOPT_E_ALIAS: return "tensor buffers overlap";
+    default: return "unknown error";
+  }
+}
+
+int lopt_weight_set_size(int d_feat, int hidden) {
+  if (d_feat != LOPT_D_FEAT || hidden < 1 || hidden > LOPT_MAX_HIDDEN) return LOPT_E_ARG;
+  return d_feat * hidden + hidden + hidden * hidden + hidden + 2 * hidden + 2;
+}
+
+int lopt_create(const float* mlp_weights, int d_feat, int hidden, int n_sets, lopt_handle* out) {
+  if (!out) return LOPT_E_ARG;
+  *out = nullptr;
+  if (!mlp_weights || n_sets < 1 || d_feat != LOPT_D_FEAT) return LOPT_E_ARG;
+  if (hidden < 1 || hidden > LOPT_MAX_HIDDEN) return LOPT_E_UNSUPPORTED;
+  const int hp = padded_hidden(hidden);
+  if (hp < 0 || !apply_fp32_supported(hp)) return LOPT_E_UNSUPPORTED;
+
+  // Re-lay the caller's sets at the padded width (extra units get zero
+  // weights and zero biases, so they contribute exactly nothing).
+  const int H = hidden, src_sz = lopt_weight_set_size(d_feat, hidden), dst_sz = w_set_size(hp);
+  std::vector<float> packed((size_t)n_sets * dst_sz, 0.f);
+  for (int s = 0; s < n_sets; ++s) {
+    const float* src = mlp_weights + (size_t)s * src_sz;
+    float* dst = packed.data() + (size_t)s * dst_sz;
+    for (int dd = 0; dd < kDFeat; ++dd)
+      for (int x = 0; x < H; ++x) dst[w_off_W1(hp) + dd * hp + x] = src[dd * H + x];
+    for (int x = 0; x < H; ++x) dst[w_off_b1(hp) + x] = src[kDFeat * H + x];
+    for (int a = 0; a < H; ++a)
+      for (int x = 0; x < H; ++x) dst[w_off_W2(hp) + a * hp + x] = src[kDFeat * H + H + a * H + x];
+    for (int x = 0; x < H; ++x) dst[w_off_b2(hp) + x] = src[kDFeat * H + H + H * H + x];
+    for (int a = 0; a < H; ++a)
+      for (int q = 0; q < 2; ++q) dst[w_off_W3(hp) + 2 * a + q] = src[kDFeat * H + 2 * H + H * H + 2 * a + q];
+    for (int q = 0; q < 2; ++q) dst[w_off_b3(hp) + q] = src[kDFeat * H + 4 * H + H * H + q];
+  }
+
+  lopt_ctx* h = new (std::nothrow) lopt_ctx();
+  if (!h) return LOPT_E_OOM;
+  h->hidden = hidden;
+  h->hp = hp;
+  h->n_sets = n_sets;
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaMalloc(&h->d_weights, packed.size() * sizeof(float));
+  if (e == cudaSuccess)
+    e = cudaMemcpy(h->d_weights, packed.data(), packed.size() * sizeof(float), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->done, cudaEventDisableTiming);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    if (h->d_weights) cudaFree(h->d_weights);
+    if (h->done) cudaEventDestroy(h->done);
+    delete h;
+    return cuda_fail(e);
+  }
+  *out = h;
+  return LOPT_OK;
+}
+
+int lopt_set_mlp_path(lopt_handle h, int path) {
+  if (!h) return LOPT_E_ARG;
+  if (path == LOPT_MLP_FP32) {
+    h->path = path;
+    return LOPT_OK;
+  }
+  if (path == LOPT_MLP_TC) {
+    if (!apply_tc_supported(h->hp)) return LOPT_E_UNSUPPORTED;
+    h->path = path;
+    return LOPT_OK;
+  }
+  return LOPT_E_ARG;
+}
+
+int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t t, float lr,
+              void* stream_ptr) {
+  if (!h || n_tensors < 0 || (n_tensors > 0 && !tensors)) return LOPT_E_ARG;
+  if (t < 1) return LOPT_E_ARG;
+  if (n_tensors == 0) return LOPT_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+
+  const bool same = h->last_path == h->path && (int)h->last_list.size() == n_tensors &&
+                    std::memcmp(h->last_list.data(), tensors, sizeof(lopt_tensor) * n_tensors) == 0;
+  if (!same) {
+    int rc = validate(h, tensors, n_tensors);
+    if (rc != LOPT_OK) return rc;
+  }
+  int prev_device = -1;
+  cudaError_t e = cudaGetDevice(&prev_device);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (prev_device != h->device) {
+    e = cudaSetDevice(h->device);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  struct Restore {
+    int dev, want;
+    ~Restore() { if (dev >= 0 && dev != want) cudaSetDevice(dev); }
+  } restore{prev_device, h->device};
+  if (h->has_done) {
+    e = cudaStreamWaitEvent(stream, h->done, 0);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if (!same) {
+    int rc = build_schedule(h, tensors, n_tensors, stream);
+    if (rc != LOPT_OK) {
+      h->last_list.clear();
+      return rc;
+    }
+  }
+
+  StepArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.desc = h->d_desc;
+  a.hidden = h->hp;
+  a.aux = h->d_aux;
+  a.colpart = h->d_colpart;
+  a.rowpart = h->d_rowpart;
+  a.k1part = h->d_k1part;
+  a.weights = h->d_weights;
+  a.set_size = w_set_size(h->hp);
+  a.w1fold = h->d_w1fold;
+  a.w1fold_stride = h->w1fold_stride;
+  a.path = h->path;
+  a.t = (double)t;
+  a.lr = lr;
+  a.status = h->d_status;
+
+  cudaEvent_t* ev = nullptr;
+  if (h->timing) {
+    if (h->tev_used + 4 > h->tev.size()) {
+      for (int k = 0; k < 4; ++k) {
+        cudaEvent_t x;
+        e = cudaEventCreate(&x);
+        if (e != cudaSuccess) return cuda_fail(e);
+        h->tev.push_back(x);
+      }
+    }
+    ev = h->tev.data() + h->tev_used;
+    h->tev_used += 4;
+  }
+  auto mark = [&](int k) {
+    if (ev && e == cudaSuccess) e = cudaEventRecord(ev[k], stream);
+  };
+
+  mark(0);
+  a.units = h->d_units[0];
+  a.n_units = h->n_units[0];
+  a.counters = h->d_counters;
+  if (e == cudaSuccess) e = launch_rowcol(a, stream);
+  mark(1);
+  if (e == cudaSuccess) {
+    a.units = h->d_units[1];
+    a.n_units = h->n_units[1];
+    a.counters = h->d_counters + n_tensors;
+    e = launch_stats(a, stream);
+  }
+  mark(2);
+  if (e == cudaSuccess) {
+    a.units = h->d_units[2];
+    a.n_units = h->n_units[2];
+    a.counters = nullptr;
+    e = (h->path == LOPT_MLP_TC) ? launch_apply_tc(a, stream) : launch_apply_fp32(a, stream);
+  }
+  mark(3);
+  if (e != cudaSuccess) {
+    h->last_list.clear();
+    return cuda_fail(e);
+  }
+  e = cudaEventRecord(h->done, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
+  h->has_done = true;
+  return LOPT_OK;
+}
+
+int lopt_check(lopt_handle h) {
+  if (!h) return LOPT_E_ARG;
+  if (!h->has_done) return LOPT_OK;
+  cudaError_t e = cudaEventSynchronize(h->done);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (!h->d_status) return LOPT_OK;
+  int32_t st = 0;
+  e = cudaMemcpy(&st, h->d_status, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (st != 0) {
+    e = cudaMemset(h->d_status, 0, sizeof(int32_t));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return LOPT_E_TIMEOUT;
+  }
+  return LOPT_OK;
+}
+
+int lopt_feature_stats(lopt_handle h, int index, double* out) {
+  if (!h || !out || index < 0 || index >= h->n_tensors) return LOPT_E_ARG;
+  if (h->has_done) {
+    cudaError_t e = cudaEventSynchronize(h->done);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  const char* src = reinterpret_cast<const char*>(h->d_aux) + sizeof(TensorAux) * (size_t)index +
+                    offsetof(TensorAux, S);
+  cudaError_t e = cudaMemcpy(out, src, sizeof(double) * kStats, cudaMemcpyDeviceToHost);
+  return e == cudaSuccess ? LOPT_OK : cuda_fail(e);
+}
+
+int lopt_set_kernel_timing(lopt_handle h, int enable) {
+  if (!h) return LOPT_E_ARG;
+  h->timing = enable != 0;
+  return LOPT_OK;
+}
+
+int lopt_kernel_times(lopt_handle h, double* ms, int64_t* launches) {
+  if (!h || !ms || !launches) return LOPT_E_ARG;
+  for (int k = 0; k < 3; ++k) {
+    ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  if (h->tev_used == 0) return LOPT_OK;
+  cudaError_t e = cudaEventSynchronize(h->tev[h->tev_used - 1]);
+  if (e != cudaSuccess) return cuda_fail(e);
+  for (size_t s = 0; s + 4 <= h->tev_used; s += 4) {
+    for (int k = 0; k < 3; ++k) {
+      float x = 0.f;
+      e = cudaEventElapsedTime(&x, h->tev[s + k], h->tev[s + k + 1]);
+      if (e != cudaSuccess) return cuda_fail(e);
+      ms[k] += x;
+      launches[k] += 1;
+    }
+  }
+  h->tev_used = 0;
+  return LOPT_OK;
+}
+
+int lopt_destroy(lopt_handle h) {
+  if (!h) return LOPT_E_ARG;
+  if (h->has_done) cudaEventSynchronize(h->done);
+  for (cudaEvent_t x : h->tev) cudaEventDestroy(x);
+  if (h->d_ws) cudaFree(h->d_ws);
+  if (h->d_weights) cudaFree(h->d_weights);
+  if (h->done) cudaEventDestroy(h->done);
+  delete h;
+  return LOPT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,237 @@
+"""Python binding of liblopt (include/lopt.h): argument marshalling only.
+
+Every step of the optimizer runs inside the library's CUDA kernels; this
+module converts torch tensors to device pointers and calls the C ABI.  There
+is no fallback: if liblopt.so is missing or a tensor is not a contiguous
+CUDA float32 tensor, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "liblopt.so")
+
+LOPT_OK = 0
+LOPT_D_FEAT = 39
+LOPT_N_STATS = 28
+MLP_FP32 = 0
+MLP_TC = 1
+_PATHS = {"fp32": MLP_FP32, "tc": MLP_TC}
+
+ERRORS = {
+    -1: "LOPT_E_ARG", -2: "LOPT_E_SHAPE", -3: "LOPT_E_ALIGN", -4: "LOPT_E_CUDA",
+    -5: "LOPT_E_OOM", -6: "LOPT_E_UNSUPPORTED", -7: "LOPT_E_TIMEOUT", -8: "LOPT_E_ALIAS",
+}
+
+EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_step",
+            "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
+            "lopt_destroy", "lopt_strerror", "lopt_version")
+
+
+class LoptTensor(ctypes.Structure):
+    """Mirror of lopt_tensor."""
+    _fields_ = [
+        ("param", ctypes.c_void_p), ("grad", ctypes.c_void_p),
+        ("mom", ctypes.c_void_p * 3), ("rms", ctypes.c_void_p),
+        ("row", ctypes.c_void_p * 3), ("col", ctypes.c_void_p * 3),
+        ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+        ("weight_set", ctypes.c_int32), ("reserved", ctypes.c_int32),
+    ]
+
+
+class LoptError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__("%s failed: %s (%s, %d)" % (fn, msg, ERRORS.get(code, "?"), code))
+        self.code = code
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load liblopt.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError("liblopt.so not found at %s; build it with "
+                          "learned_optimizer_step_gb300.build.build()" % path)
+    lib = ctypes.CDLL(path)
+    vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    lib.lopt_weight_set_size.argtypes = [i32, i32]
+    lib.lopt_weight_set_size.restype = i32
+    lib.lopt_create.argtypes = [ctypes.POINTER(ctypes.c_float), i32, i32, i32, ctypes.POINTER(vp)]
+    lib.lopt_create.restype = i32
+    lib.lopt_set_mlp_path.argtypes = [vp, i32]
+    lib.lopt_set_mlp_path.restype = i32
+    lib.lopt_step.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, i64, ctypes.c_float, vp]
+    lib.lopt_step.restype = i32
+    lib.lopt_check.argtypes = [vp]
+    lib.lopt_check.restype = i32
+    lib.lopt_feature_stats.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double)]
+    lib.lopt_feature_stats.restype = i32
+    lib.lopt_set_kernel_timing.argtypes = [vp, i32]
+    lib.lopt_set_kernel_timing.restype = i32
+    lib.lopt_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
+    lib.lopt_kernel_times.restype = i32
+    lib.lopt_destroy.argtypes = [vp]
+    lib.lopt_destroy.restype = i32
+    lib.lopt_strerror.argtypes = [i32]
+    lib.lopt_strerror.restype = ctypes.c_char_p
+    lib.lopt_version.argtypes = []
+    lib.lopt_version.restype = i32
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, code: int) -> None:
+    if code != LOPT_OK:
+        raise LoptError(fn, code, load_library().lopt_strerror(code).decode())
+
+
+def _ptr(t, n: int, what: str) -> int:
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % what)
+    if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous CUDA float32 tensor" % what)
+    if t.numel() != n:
+        raise ValueError("%s has %d elements, expected %d" % (what, t.numel(), n))
+    return t.data_ptr()
+
+
+@dataclass
+class TensorState:
+    """One parameter tensor and its optimizer state (all CUDA float32)."""
+    param: "object"
+    grad: "object"
+    mom: List["object"]
+    rms: "object"
+    row: List["object"]
+    col: List["object"]
+    rows: int
+    cols: int
+    weight_set: int = 0
+
+    @staticmethod
+    def from_dict(d: dict) -> "TensorState":
+        return TensorState(d["param"], d["grad"], list(d["mom"]), d["rms"], list(d["row"]),
+                           list(d["col"]), int(d["rows"]), int(d["cols"]), int(d.get("weight_set", 0)))
+
+    def to_c(self) -> LoptTensor:
+        n = self.rows * self.cols
+        c = LoptTensor()
+        c.param = _ptr(self.param, n, "param")
+        c.grad = _ptr(self.grad, n, "grad")
+        for k in range(3):
+            c.mom[k] = _ptr(self.mom[k], n, "mom[%d]" % k)
+            c.row[k] = _ptr(self.row[k], self.rows, "row[%d]" % k)
+            c.col[k] = _ptr(self.col[k], self.cols, "col[%d]" % k)
+        c.rms = _ptr(self.rms, n, "rms")
+        c.rows, c.cols, c.weight_set, c.reserved = self.rows, self.cols, self.weight_set, 0
+        return c
+
+
+class PreparedList:
+    """A parameter list marshalled once into the C descriptor array."""
+
+    def __init__(self, tensors: Sequence[TensorState]):
+        self.tensors = list(tensors)
+        self.array = (LoptTensor * len(self.tensors))(*[t.to_c() for t in self.tensors])
+        self.n = len(self.tensors)
+        self.numel = sum(t.rows * t.cols for t in self.tensors)
+
+
+def weight_set_size(hidden: int) -> int:
+    n = load_library().lopt_weight_set_size(LOPT_D_FEAT, int(hidden))
+    if n < 0:
+        _check("lopt_weight_set_size", n)
+    return n
+
+
+class LearnedOptimizer:
+    """One library handle: MLP weight sets + workspace.  ``step`` runs one
+    learned-optimizer step over a whole parameter list."""
+
+    def __init__(self, weights: np.ndarray, hidden: int = 32, mlp_path: str = "fp32"):
+        lib = load_library()
+        w = np.ascontiguousarray(np.asarray(weights, dtype=np.float32))
+        size = weight_set_size(hidden)
+        if w.size % size != 0 or w.size == 0:
+            raise ValueError("weights must hold n_sets * %d floats" % size)
+        self.hidden = int(hidden)
+        self.n_sets = w.size // size
+        self._w = w
+        h = ctypes.c_void_p()
+        _check("lopt_create", lib.lopt_create(w.ctypes.data_as(ctypes.POINTER(ctypes.c_float)),
+                                              LOPT_D_FEAT, self.hidden, self.n_sets, ctypes.byref(h)))
+        self._h = h
+        self.set_mlp_path(mlp_path)
+
+    def set_mlp_path(self, path: str) -> None:
+        _check("lopt_set_mlp_path", load_library().lopt_set_mlp_path(self._h, _PATHS[path]))
+        self.mlp_path = path
+
+    def prepare(self, tensors: Sequence) -> PreparedList:
+        ts = [t if isinstance(t, TensorState) else TensorState.from_dict(t) for t in tensors]
+        return PreparedList(ts)
+
+    def step(self, tensors, t: int, lr: float = 1.0, stream: Optional[object] = None) -> None:
+        """Enqueue one step (asynchronous on ``stream``; default: torch's
+        current stream)."""
+        import torch
+        pl = tensors if isinstance(tensors, PreparedList) else self.prepare(tensors)
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+        _check("lopt_step", load_library().lopt_step(self._h, pl.array, pl.n, int(t), float(lr),
+                                                      ctypes.c_void_p(handle)))
+
+    def check(self) -> None:
+        """Wait for the last step; raise if a kernel reported an error."""
+        _check("lopt_check", load_library().lopt_check(self._h))
+
+    def feature_stats(self, index: int) -> np.ndarray:
+        out = np.zeros(LOPT_N_STATS, dtype=np.float64)
+        _check("lopt_feature_stats", load_library().lopt_feature_stats(
+            self._h, int(index), out.ctypes.data_as(ctypes.POINTER(ctypes.c_double))))
+        return out
+
+    def set_kernel_timing(self, enable: bool) -> None:
+        _check("lopt_set_kernel_timing", load_library().lopt_set_kernel_timing(self._h, int(enable)))
+
+    def kernel_times(self):
+        """(ms[3], launches[3]) summed since the last call: row/column,
+        statistics and apply kernels."""
+        ms = (ctypes.c_double * 3)()
+        n = (ctypes.c_int64 * 3)()
+        _check("lopt_kernel_times", load_library().lopt_kernel_times(self._h, ms, n))
+        return list(ms), list(n)
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            load_library().lopt_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def zeros_state(param, grad, rows: int, cols: int, weight_set: int = 0) -> TensorState:
+    """State for ``param`` with zero accumulators (allocated like ``param``)."""
+    import torch
+    n = rows * cols
+    z = lambda m: torch.zeros(m, device=param.device, dtype=torch.float32)
+    return TensorState(param.reshape(-1), grad.reshape(-1), [z(n) for _ in range(3)], z(n),
+                       [z(rows) for _ in range(3)], [z(cols) for _ in range(3)], rows, cols,
+                       weight_set)

@@ -1,0 +1,85 @@
+"""CPU checks of the C ABI: the library loads, exports every function that
+include/lopt.h declares, and argument validation that needs no device
+returns the documented error codes.  No compute call is made."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from learned_optimizer_step_gb300 import build as B
+from learned_optimizer_step_gb300 import lopt as L
+
+HEADER = os.path.join(B.ROOT, "include", "lopt.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return L.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lopt_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("lopt_create", "lopt_step", "lopt_destroy", "lopt_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), "liblopt.so does not export " + name
+    assert sorted(declared_functions()) == sorted(L.EXPORTED)
+
+
+def test_struct_layout_matches_header():
+    # 12 pointers, two int64 and two int32, natural alignment, no padding
+    assert ctypes.sizeof(L.LoptTensor) == 12 * 8 + 2 * 8 + 2 * 4
+    assert L.LoptTensor.rows.offset == 96
+
+
+def test_error_strings(lib):
+    for code, name in L.ERRORS.items():
+        s = lib.lopt_strerror(code).decode()
+        assert s and s != "unknown error", name
+    assert lib.lopt_strerror(0).decode() == "ok"
+    assert lib.lopt_version() >= 100
+
+
+def test_weight_set_size(lib):
+    assert lib.lopt_weight_set_size(39, 32) == 39 * 32 + 32 + 32 * 32 + 32 + 64 + 2
+    assert lib.lopt_weight_set_size(39, 4) == 39 * 4 + 4 + 16 + 4 + 8 + 2
+    assert lib.lopt_weight_set_size(30, 32) == -1
+    assert lib.lopt_weight_set_size(39, 0) == -1
+
+
+def test_validation_before_any_device_call(lib):
+    h = ctypes.c_void_p()
+    w = (ctypes.c_float * 10)()
+    fp = ctypes.cast(w, ctypes.POINTER(ctypes.c_float))
+    assert lib.lopt_create(fp, 39, 32, 1, None) == -1
+    assert lib.lopt_create(None, 39, 32, 1, ctypes.byref(h)) == -1
+    assert lib.lopt_create(fp, 30, 32, 1, ctypes.byref(h)) == -1
+    assert lib.lopt_create(fp, 39, 32, 0, ctypes.byref(h)) == -1
+    assert lib.lopt_create(fp, 39, 65, 1, ctypes.byref(h)) == -6
+    assert h.value is None
+    assert lib.lopt_step(None, None, 0, 1, 1.0, None) == -1
+    assert lib.lopt_check(None) == -1
+    assert lib.lopt_destroy(None) == -1
+    assert lib.lopt_set_mlp_path(None, 0) == -1
+    assert lib.lopt_feature_stats(None, 0, None) == -1
+    assert lib.lopt_set_kernel_timing(None, 1) == -1
+    assert lib.lopt_kernel_times(None, None, None) == -1
+
+
+def test_binding_rejects_non_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    t = torch.zeros(4)
+    with pytest.raises(TypeError):
+        L._ptr(t, 4, "param")

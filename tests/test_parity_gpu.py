@@ -1,0 +1,242 @@
+"""GPU parity of lopt_step (through the C ABI) against the CPU oracle.
+
+Every test feeds identical seeded inputs to both sides and compares element
+by element (small cases) or at sampled elements plus the whole-tensor
+statistics and accumulators (full-size lists).  Tolerances: 1e-5 relative on
+updated parameters for the FP32 MLP path, 2e-3 for the tensor-core path
+(relative to max(|oracle value|, RMS of the tensor's oracle values)); 2e-6
+on accumulators; 2e-5 on the per-feature sums of squares."""
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from tests.gpu_helpers import (TOL_FP32, TOL_TC, compare_step, cpu, make_states, need_gpu,
+                               rel_err, to_oracle)
+
+pytestmark = pytest.mark.gpu
+
+EDGE_SHAPES = [("one", (1,)), ("scalar", ()), ("row5", (5,)), ("col7", (7, 1)),
+               ("odd", (3, 5)), ("ragged", (33, 129)), ("long", (3072,)),
+               ("head", (5, 1000)), ("tall", (1100, 3)), ("cube", (2, 3, 4)),
+               ("w", (64, 96))]
+
+
+def engine(hidden=32, n_sets=1, path="fp32", seed=1234):
+    need_gpu()
+    from learned_optimizer_step_gb300 import LearnedOptimizer
+    w = synth.make_weight_sets(n_sets, hidden, seed=seed)
+    return LearnedOptimizer(w, hidden, path), w
+
+
+@pytest.mark.parametrize("path,tol", [("fp32", TOL_FP32)])
+def test_single_256x256_three_steps(path, tol):
+    torch = need_gpu()
+    eng, w = engine(path=path)
+    wl = synth.workloads()["single_256x256"]
+    states = synth.make_list(wl, "cuda", seed=0)
+    for step in range(wl.steps):
+        if step > 0:
+            synth.refresh_grads(states, wl, step)
+        compare_step(eng, states, w, 32, wl.first_step + step, 1.0, tol)
+
+
+@pytest.mark.parametrize("hidden", [4, 32])
+def test_edge_shapes_per_tensor_weights(hidden):
+    need_gpu()
+    eng, w = engine(hidden=hidden, n_sets=len(EDGE_SHAPES))
+    states = make_states(EDGE_SHAPES, recipe="vit", seed=3, per_tensor_weights=True)
+    for t in (1, 2):
+        compare_step(eng, states, w, hidden, t, 0.5, TOL_FP32)
+
+
+def test_odd_hidden_width_is_padded_exactly():
+    need_gpu()
+    eng, w = engine(hidden=5, n_sets=1)
+    states = make_states([("a", (17, 31)), ("b", (40,))], recipe="vit", seed=4)
+    compare_step(eng, states, w, 5, 1, 1.0, TOL_FP32)
+
+
+def test_ragged_launch_equals_solo_launches_bitwise():
+    torch = need_gpu()
+    eng, w = engine(n_sets=1)
+    a = make_states(EDGE_SHAPES, recipe="vit", seed=5)
+    b = make_states(EDGE_SHAPES, recipe="vit", seed=5)
+    eng.step(a, 3, 1.0)
+    for s in b:
+        eng.step([s], 3, 1.0)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        for k in ("param", "rms"):
+            assert torch.equal(x[k], y[k]), x["name"]
+        for k in ("mom", "row", "col"):
+            for u, v in zip(x[k], y[k]):
+                assert torch.equal(u, v), x["name"]
+
+
+def test_two_runs_are_bitwise_identical():
+    torch = need_gpu()
+    eng, w = engine()
+    shapes = [("a", (300, 700)), ("b", (700,)), ("c", (2048, 96))]
+    a = make_states(shapes, recipe="vit", seed=6)
+    b = make_states(shapes, recipe="vit", seed=6)
+    for t in (1, 2):
+        eng.step(a, t, 1.0)
+        eng.step(b, t, 1.0)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x["param"], y["param"])
+        assert torch.equal(x["mom"][2], y["mom"][2])
+
+
+def test_misaligned_views_take_the_scalar_path():
+    torch = need_gpu()
+    eng, w = engine()
+    base = make_states([("w", (40, 64))], recipe="vit", seed=7)[0]
+    st = {}
+    n = base["rows"] * base["cols"]
+    for k in ("param", "grad", "rms"):
+        buf = torch.zeros(n + 1, device="cuda")
+        buf[1:].copy_(base[k])
+        st[k] = buf[1:]                      # 4-byte aligned, not 16-byte
+    st["mom"] = []
+    for m in base["mom"]:
+        buf = torch.zeros(n + 1, device="cuda")
+        buf[1:].copy_(m)
+        st["mom"].append(buf[1:])
+    st.update(row=base["row"], col=base["col"], rows=40, cols=64, weight_set=0, name="mis")
+    compare_step(eng, [st], w, 32, 1, 1.0, TOL_FP32)
+
+
+def test_validation_leaves_state_untouched():
+    torch = need_gpu()
+    from learned_optimizer_step_gb300 import LoptError
+    eng, w = engine()
+    st = make_states([("w", (16, 16))], recipe="vit", seed=8)[0]
+    before = st["param"].clone()
+    bad = dict(st)
+    bad["mom"] = [st["mom"][0], st["mom"][0], st["mom"][2]]   # aliasing
+    with pytest.raises(LoptError) as ei:
+        eng.step([bad], 1, 1.0)
+    assert ei.value.code == -8
+    bad = dict(st)
+    bad["weight_set"] = 3
+    with pytest.raises(LoptError) as ei:
+        eng.step([bad], 1, 1.0)
+    assert ei.value.code == -1
+    torch.cuda.synchronize()
+    assert torch.equal(before, st["param"])
+
+
+def test_resume_from_saved_state_is_bitwise_identical():
+    torch = need_gpu()
+    eng, w = engine()
+    shapes = [("a", (64, 80)), ("b", (80,))]
+    wl = synth.Workload("r", tuple(shapes), 4, 1, "vit")
+    a = synth.make_list(wl, "cuda", seed=9)
+    for t in (1, 2):
+        synth.refresh_grads(a, wl, t)
+        eng.step(a, t, 1.0)
+    saved = [{k: (v.clone() if hasattr(v, "clone") else [x.clone() for x in v] if isinstance(v, list) else v)
+              for k, v in s.items()} for s in a]
+    eng2, _ = engine()
+    for t in (3, 4):
+        synth.refresh_grads(a, wl, t)
+        synth.refresh_grads(saved, wl, t)
+        eng.step(a, t, 1.0)
+        eng2.step(saved, t, 1.0)
+    torch.cuda.synchronize()
+    for x, y in zip(a, saved):
+        assert torch.equal(x["param"], y["param"])
+
+
+def test_identity_mlp_is_normalised_sgd_on_gpu():
+    """Closed form on the GPU: routing weights make the step normalised SGD."""
+    torch = need_gpu()
+    from learned_optimizer_step_gb300 import LearnedOptimizer
+    H = 32
+    W1 = np.zeros((39, H)); W1[1, 0] = 1.0; W1[1, 1] = -1.0
+    W2 = np.zeros((H, H)); W2[0, 0] = 1.0; W2[1, 1] = 1.0
+    W3 = np.zeros((H, 2)); W3[0, 0] = 1.0; W3[1, 0] = -1.0
+    wf = np.concatenate([W1.ravel(), np.zeros(H), W2.ravel(), np.zeros(H), W3.ravel(),
+                         [0.0, 300.0]]).astype(np.float32)
+    eng = LearnedOptimizer(wf, H, "fp32")
+    st = make_states([("w", (128, 256))], recipe="vit", seed=10)[0]
+    p0 = cpu(st["param"]); g = cpu(st["grad"])
+    eng.step([st], 1, 0.25)
+    torch.cuda.synchronize()
+    expect = p0 - 0.25 * 1e-3 * np.exp(0.3) * g / np.sqrt(np.mean(g * g) + 1e-30)
+    assert rel_err(cpu(st["param"]), expect) < 1e-5
+
+
+def _sample(n_per=512, seed=0):
+    rng = np.random.default_rng(seed)
+
+    def pick(st):
+        n = st["rows"] * st["cols"]
+        if n <= 4 * n_per:
+            return np.arange(n)
+        idx = rng.choice(n, size=n_per, replace=False)
+        return np.unique(np.concatenate([idx, [0, n - 1]]))
+    return pick
+
+
+def _unique_shape_subset(states):
+    seen, out = set(), []
+    for s in states:
+        key = (s["rows"], s["cols"], s["name"].split(".")[-1])
+        if key not in seen:
+            seen.add(key)
+            out.append(s)
+    return out
+
+
+def test_vit_b16_full_size_sampled():
+    """Full ViT-B/16 list in one launch per kernel; every tensor's stats and
+    accumulators are compared in full, parameters at sampled elements, for
+    one tensor of each distinct shape."""
+    torch = need_gpu()
+    eng, w = engine()
+    wl = synth.workloads()["vit_b16"]
+    states = synth.make_list(wl, "cuda", seed=0)
+    ref_states = _unique_shape_subset(states)
+    ref = {id(s): to_oracle(s) for s in ref_states}
+    eng.step(states, 1, 1.0)
+    eng.check()
+    torch.cuda.synchronize()
+    ws = O.unpack_weights(w[0], 32)
+    pick = _sample()
+    for idx, st in enumerate(states):
+        if id(st) not in ref:
+            continue
+        r = ref[id(st)]
+        sidx = pick(st)
+        out = O.step_tensor(r, 1, 1.0, ws, sample_idx=sidx)
+        assert rel_err(cpu(st["param"])[sidx], out["sample_param"]) <= TOL_FP32, st["name"]
+        assert rel_err(eng.feature_stats(idx), out["S"], floor=1e-300) <= 2e-5, st["name"]
+        assert rel_err(cpu(st["mom"][1]), r["mom"][1]) <= 2e-6
+        assert rel_err(cpu(st["col"][0]), r["col"][0]) <= 2e-6, st["name"]
+
+
+def test_gpt2_heavy_tails_late_step_sampled():
+    """GPT-2-small list, Student-t gradients, t = 9991 with warmed-up
+    accumulators; checks the token embedding and one tensor per shape."""
+    torch = need_gpu()
+    eng, w = engine()
+    wl = synth.workloads()["gpt2_small"]
+    states = synth.make_list(wl, "cuda", seed=0)
+    ref_states = _unique_shape_subset(states)
+    ref = {id(s): to_oracle(s) for s in ref_states}
+    eng.step(states, wl.first_step, 1.0)
+    torch.cuda.synchronize()
+    ws = O.unpack_weights(w[0], 32)
+    pick = _sample(seed=1)
+    for idx, st in enumerate(states):
+        if id(st) not in ref:
+            continue
+        r = ref[id(st)]
+        sidx = pick(st)
+        out = O.step_tensor(r, wl.first_step, 1.0, ws, sample_idx=sidx)
+        assert rel_err(cpu(st["param"])[sidx], out["sample_param"]) <= TOL_FP32, st["name"]
+        assert rel_err(eng.feature_stats(idx), out["S"], floor=1e-300) <= 2e-5, st["name"]
