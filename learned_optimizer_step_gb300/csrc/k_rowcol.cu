@@ -23,7 +23,6 @@ namespace {
 constexpr int kT = kRowColThreads;
 constexpr int kWarps = kT / 32;
 constexpr int kRowBatch = 8;         // rows reduced together
-constexpr int kMaxStripRows = 512;   // host guarantees strip_rows <= this
 
 template <int W>   // W = 4: float4 columns, W = 1: scalar columns
 __device__ void strip_pass(const TensorDesc& d, int64_t r0, int nrows, float* colpart_strip,
@@ -148,16 +147,43 @@ __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
   if (!is_last) return;
   __threadfence();
 
+  // Column means: every thread owns whole columns and sums their strip
+  // partials in strip order (four independent columns per thread when the
+  // tensor allows 128-bit access, to keep many loads in flight).
   const float* cp = a.colpart + d.colpart_off;
   const double invR = 1.0 / (double)d.R;
-  for (int64_t j = tid; j < d.C; j += kT) {
-    double s = 0.0;
-    for (int st = 0; st < d.n_strips; ++st) s += (double)__ldcg(cp + (int64_t)st * d.C + j);
-    const float H = (float)(s * invR);
+  const int S = d.n_strips;
+  if (d.vec4 && (d.C % 4 == 0)) {
+    for (int64_t j = 4 * (int64_t)tid; j < d.C; j += 4 * (int64_t)kT) {
+      double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+#pragma unroll 8
+      for (int st = 0; st < S; ++st) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(cp + (int64_t)st * d.C + j));
+        s0 += (double)x.x; s1 += (double)x.y; s2 += (double)x.z; s3 += (double)x.w;
+      }
+      const float H[4] = {(float)(s0 * invR), (float)(s1 * invR), (float)(s2 * invR), (float)(s3 * invR)};
 #pragma unroll
-    for (int k = 0; k < 3; ++k) {
-      float* c = d.c[k] + j;
-      *c = ffma(beta(k), *c, fmul(one_minus_beta(k), H));
+      for (int k = 0; k < 3; ++k) {
+        float4* c4 = reinterpret_cast<float4*>(d.c[k] + j);
+        float4 c = *c4;
+        c.x = ffma(beta(k), c.x, fmul(one_minus_beta(k), H[0]));
+        c.y = ffma(beta(k), c.y, fmul(one_minus_beta(k), H[1]));
+        c.z = ffma(beta(k), c.z, fmul(one_minus_beta(k), H[2]));
+        c.w = ffma(beta(k), c.w, fmul(one_minus_beta(k), H[3]));
+        *c4 = c;
+      }
+    }
+  } else {
+    for (int64_t j = tid; j < d.C; j += kT) {
+      double s = 0.0;
+#pragma unroll 8
+      for (int st = 0; st < S; ++st) s += (double)__ldcg(cp + (int64_t)st * d.C + j);
+      const float H = (float)(s * invR);
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        float* c = d.c[k] + j;
+        *c = ffma(beta(k), *c, fmul(one_minus_beta(k), H));
+      }
     }
   }
   if (tid < 3) {

@@ -33,6 +33,7 @@ struct lopt_ctx {
   int n_sets = 0;
   int path = LOPT_MLP_FP32;
   float* d_weights = nullptr;  // [n_sets][w_set_size(hp)], zero-padded
+  void* d_tcw = nullptr;       // packed FP16 layer-2/3 operands (tensor-core path)
   // workspace
   char* d_ws = nullptr;
   size_t ws_bytes = 0;
@@ -112,13 +113,16 @@ int validate(const lopt_ctx* h, const lopt_tensor* ts, int n) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-// Rows per K0 strip: about kStripTarget elements, at most kMaxStrips strips,
-// at most 512 rows (the kernel's shared row buffer).
+// Rows per K0 strip.  About kStripTarget elements per strip, but no more
+// than kFinalizeCap / cols strips (the last block of a tensor sums
+// strips x cols column partials) and no more than kMaxStripRows rows.
 int strip_rows_for(int64_t R, int64_t C) {
-  int64_t rows = std::max<int64_t>(1, kStripTarget / std::max<int64_t>(C, 1));
-  rows = std::max<int64_t>(rows, (R + kMaxStrips - 1) / kMaxStrips);
-  rows = std::min<int64_t>(rows, 512);
-  rows = std::min<int64_t>(rows, R);
+  const int64_t N = R * C;
+  int64_t strips = std::max<int64_t>(1, (N + kStripTarget - 1) / kStripTarget);
+  strips = std::min<int64_t>(strips, std::max<int64_t>(1, kFinalizeCap / std::max<int64_t>(C, 1)));
+  strips = std::min<int64_t>(strips, R);
+  int64_t rows = (R + strips - 1) / strips;
+  rows = std::min<int64_t>(rows, kMaxStripRows);
   return (int)std::max<int64_t>(rows, 1);
 }
 
@@ -149,6 +153,7 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
     d.n_strips = (int)((d.R + d.strip_rows - 1) / d.strip_rows);
     d.k1_units = (int)((d.N + kStatsChunk - 1) / kStatsChunk);
     d.k2_units = (int)((d.N + kApplyChunk - 1) / kApplyChunk);
+    colpart = (colpart + 3) / 4 * 4;   // 16-byte aligned start for float4 reads
     d.colpart_off = colpart;
     colpart += (int64_t)d.n_strips * d.C;
     d.rowpart_off = (int32_t)rowpart;
@@ -293,8 +298,14 @@ int lopt_create(const float* mlp_weights, int d_feat, int hidden, int n_sets, lo
   if (e == cudaSuccess)
     e = cudaMemcpy(h->d_weights, packed.data(), packed.size() * sizeof(float), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->done, cudaEventDisableTiming);
+  if (e == cudaSuccess && apply_tc_supported(hp)) {
+    e = cudaMalloc(&h->d_tcw, tc_weights_bytes(hp, n_sets));
+    if (e == cudaSuccess) e = pack_tc_weights(h->d_weights, hp, n_sets, h->d_tcw, 0);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  }
   if (e != cudaSuccess) {
     cudaGetLastError();
+    if (h->d_tcw) cudaFree(h->d_tcw);
     if (h->d_weights) cudaFree(h->d_weights);
     if (h->done) cudaEventDestroy(h->done);
     delete h;
@@ -311,7 +322,7 @@ int lopt_set_mlp_path(lopt_handle h, int path) {
     return LOPT_OK;
   }
   if (path == LOPT_MLP_TC) {
-    if (!apply_tc_supported(h->hp)) return LOPT_E_UNSUPPORTED;
+    if (!apply_tc_supported(h->hp) || !h->d_tcw) return LOPT_E_UNSUPPORTED;
     h->path = path;
     return LOPT_OK;
   }
@@ -367,6 +378,7 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   a.w1fold = h->d_w1fold;
   a.w1fold_stride = h->w1fold_stride;
   a.path = h->path;
+  a.tc_weights = h->d_tcw;
   a.t = (double)t;
   a.lr = lr;
   a.status = h->d_status;
@@ -481,6 +493,7 @@ int lopt_destroy(lopt_handle h) {
   for (cudaEvent_t x : h->tev) cudaEventDestroy(x);
   if (h->d_ws) cudaFree(h->d_ws);
   if (h->d_weights) cudaFree(h->d_weights);
+  if (h->d_tcw) cudaFree(h->d_tcw);
   if (h->done) cudaEventDestroy(h->done);
   delete h;
   return LOPT_OK;

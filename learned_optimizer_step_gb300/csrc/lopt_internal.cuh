@@ -6,6 +6,7 @@
 // defaults (see the comment on lopt_features below).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -36,8 +37,9 @@ constexpr int kStatsThreads  = 256;   // K1 block
 constexpr int kStatsChunk    = 16384; // elements per K1 work unit
 constexpr int kApplyThreads  = 128;   // K2 (FP32 MLP) block
 constexpr int kApplyChunk    = 4096;  // elements per K2 work unit
-constexpr int kMaxStrips     = 128;   // K0 strips per tensor (column partials)
 constexpr int kStripTarget   = 32768; // elements per K0 strip, when possible
+constexpr int kFinalizeCap   = 65536; // K0: strips * cols bound (column partials one block sums)
+constexpr int kMaxStripRows  = 2048;  // K0: rows of one strip (shared row buffer)
 
 // One tensor of a step, as the kernels see it.
 struct TensorDesc {
@@ -88,6 +90,7 @@ struct StepArgs {
   float*            w1fold;      // [T][w1fold_stride] per-tensor folded W1, b1
   int32_t           w1fold_stride;
   int32_t           path;        // LOPT_MLP_*
+  const void*       tc_weights;  // per-set packed FP16 B operands (tensor-core path)
   double            t;           // step count
   float             lr;
   int32_t*          status;      // device-side error flags
@@ -174,5 +177,7 @@ cudaError_t launch_apply_fp32(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_apply_tc(const StepArgs& a, cudaStream_t s);
 bool apply_tc_supported(int hidden);
 int  w1fold_floats(int hidden, int path);
+size_t tc_weights_bytes(int hidden, int n_sets);
+cudaError_t pack_tc_weights(const float* weights, int hidden, int n_sets, void* out, cudaStream_t s);
 
 }  // namespace lopt

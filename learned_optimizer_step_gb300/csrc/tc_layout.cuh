@@ -1,7 +1,204 @@
-// Operand layouts of the tensor-core apply path (placeholder).
+// Tensor-core (tcgen05) helpers and operand layouts of the apply pass.
+//
+// The per-element MLP is evaluated as three batched GEMMs over a tile of 128
+// elements (one element per TMEM lane / accumulator row):
+//   layer 1  [128 x 32] (28 features, a constant-1 bias column, 3 zeros, TF32)
+//            x [32 x NP] (folded W1 and b1, TF32)
+//   layer 2  [128 x K2] (ReLU(h1) as FP16, a constant-1 column, zeros)
+//            x [K2 x NP] (W2 and b2, FP16)
+//   layer 3  [128 x K2] (ReLU(h2) as FP16, constant-1, zeros)
+//            x [K2 x 16] (W3 and b3 in the first two columns, FP16)
+// NP = hidden width padded to a multiple of 16 (>= 16), K2 = NP + 1 padded to
+// a multiple of 16.  Accumulation is FP32 in tensor memory.
+//
+// Operands live in shared memory in the canonical K-major layout without
+// swizzle: 8-row x 16-byte core matrices, core matrices adjacent along K 128
+// bytes apart (leading-dimension byte offset), 8-row groups SBO bytes apart.
 #pragma once
+
+#include <cstdint>
 #include "lopt_internal.cuh"
 
 namespace lopt {
-__device__ inline void fold_w1_tc(int, const float*, const float*, const double*, double, float*) {}
+
+__host__ __device__ constexpr int tc_np(int hp) { return hp < 16 ? 16 : (hp + 15) / 16 * 16; }
+__host__ __device__ constexpr int tc_k2(int np) { return (np + 1 + 15) / 16 * 16; }
+
+// Element offsets inside one canonical operand (row r of the M/N side, k on K).
+__host__ __device__ constexpr int tf32_off(int r, int k) {         // K = 32, 4-byte elements
+  return (r >> 3) * 256 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3);
+}
+__host__ __device__ constexpr int f16_off(int r, int k, int K) {   // 2-byte elements
+  return (r >> 3) * (K * 8) + (k >> 3) * 64 + (r & 7) * 8 + (k & 7);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float tf32_round(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
+// Shared-memory matrix descriptor: start, LBO, SBO (bytes, 16-byte units),
+// fixed version bits 46-47 = 1, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Instruction descriptor, dense, FP32 accumulator, both operands K-major.
+// fmt: 0 = f16, 2 = tf32 (kind::f16 / kind::tf32).
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t fmt, int M, int N) {
+  return (1u << 4) | (fmt << 7) | (fmt << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}\n"
+      :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n"
+      :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(smem_u32(slot)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bits, repeated 16 / 32 times along columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+}
+
+// ReLU + round-to-nearest FP16 of two floats, packed (lo = a, hi = b).
+__device__ __forceinline__ uint32_t relu_f16x2(float a, float b) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.relu.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+  return d;
+}
+
+// Prefetch `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t x, uint32_t y, uint32_t z,
+                                             uint32_t w) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(x), "r"(y), "r"(z),
+               "r"(w) : "memory");
+}
+
+// mbarrier with a bounded wait: gives up after `limit_ns` of %globaltimer.
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
+// Fold the per-tensor normalisation and the time features into layer 1 and
+// store it as the canonical TF32 B operand [NP x 32]:
+//   B[n][k] = s_k * W1[k][n] (k < 28),  b1[n] + sum_s tau_s W1[28+s][n] (k = 28),
+//   0 otherwise or for padded units n >= hp.
+__device__ inline void fold_w1_tc(int hp, const float* W1, const float* b1, const double* scale,
+                                  double t, float* out) {
+  const int np = tc_np(hp);
+  for (int x = threadIdx.x; x < np * 32; x += blockDim.x) {
+    const int n = x >> 5, k = x & 31;
+    double v = 0.0;
+    if (n < hp) {
+      if (k < kStats) {
+        v = scale[k] * (double)W1[k * hp + n];
+      } else if (k == kStats) {
+        v = (double)b1[n];
+        for (int s = 0; s < kTimeFeat; ++s) v += tanh(t / time_scale(s)) * (double)W1[(kStats + s) * hp + n];
+      }
+    }
+    out[tf32_off(n, k)] = tf32_round((float)v);
+  }
+}
+
 }  // namespace lopt

@@ -73,6 +73,12 @@ def decoder_1p3b_shapes() -> List[Tuple[str, Shape]]:
     return out
 
 
+def vit_block_shapes() -> List[Tuple[str, Shape]]:
+    """Patch embedding plus the first ViT-B/16 block (14 tensors, 7.68M
+    elements): a small case for profiler captures (state > L2)."""
+    return vit_b16_shapes()[:14]
+
+
 def velo_style_shapes() -> List[Tuple[str, Shape]]:
     """The ViT-B/16 list plus one 50,000 x 1,000 (50M-element) tensor."""
     return vit_b16_shapes() + [("big", (50000, 1000))]
@@ -102,6 +108,7 @@ def workloads() -> Dict[str, Workload]:
     return {
         "single_256x256": Workload("single_256x256", (("w", (256, 256)),), 3, 1, "single"),
         "vit_b16": Workload("vit_b16", tuple(vit_b16_shapes()), 10, 1, "vit"),
+        "vit_block": Workload("vit_block", tuple(vit_block_shapes()), 10, 1, "vit"),
         "gpt2_small": Workload("gpt2_small", tuple(gpt2_small_shapes()), 10, 9991, "gpt2"),
         "decoder_1p3b": Workload("decoder_1p3b", tuple(decoder_1p3b_shapes()), 5, 1, "vit"),
         "velo_h32": Workload("velo_h32", tuple(velo_style_shapes()), 10, 1, "vit", True, 32),

@@ -30,7 +30,10 @@ def engine(hidden=32, n_sets=1, path="fp32", seed=1234):
     return LearnedOptimizer(w, hidden, path), w
 
 
-@pytest.mark.parametrize("path,tol", [("fp32", TOL_FP32)])
+PATHS = [("fp32", TOL_FP32), ("tc", TOL_TC)]
+
+
+@pytest.mark.parametrize("path,tol", PATHS)
 def test_single_256x256_three_steps(path, tol):
     torch = need_gpu()
     eng, w = engine(path=path)
@@ -42,25 +45,28 @@ def test_single_256x256_three_steps(path, tol):
         compare_step(eng, states, w, 32, wl.first_step + step, 1.0, tol)
 
 
-@pytest.mark.parametrize("hidden", [4, 32])
-def test_edge_shapes_per_tensor_weights(hidden):
+@pytest.mark.parametrize("path,tol", PATHS)
+@pytest.mark.parametrize("hidden", [4, 32, 64])
+def test_edge_shapes_per_tensor_weights(hidden, path, tol):
     need_gpu()
-    eng, w = engine(hidden=hidden, n_sets=len(EDGE_SHAPES))
+    eng, w = engine(hidden=hidden, n_sets=len(EDGE_SHAPES), path=path)
     states = make_states(EDGE_SHAPES, recipe="vit", seed=3, per_tensor_weights=True)
     for t in (1, 2):
-        compare_step(eng, states, w, hidden, t, 0.5, TOL_FP32)
+        compare_step(eng, states, w, hidden, t, 0.5, tol)
 
 
-def test_odd_hidden_width_is_padded_exactly():
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_odd_hidden_width_is_padded_exactly(path, tol):
     need_gpu()
-    eng, w = engine(hidden=5, n_sets=1)
+    eng, w = engine(hidden=5, n_sets=1, path=path)
     states = make_states([("a", (17, 31)), ("b", (40,))], recipe="vit", seed=4)
-    compare_step(eng, states, w, 5, 1, 1.0, TOL_FP32)
+    compare_step(eng, states, w, 5, 1, 1.0, tol)
 
 
-def test_ragged_launch_equals_solo_launches_bitwise():
+@pytest.mark.parametrize("path", ["fp32", "tc"])
+def test_ragged_launch_equals_solo_launches_bitwise(path):
     torch = need_gpu()
-    eng, w = engine(n_sets=1)
+    eng, w = engine(n_sets=1, path=path)
     a = make_states(EDGE_SHAPES, recipe="vit", seed=5)
     b = make_states(EDGE_SHAPES, recipe="vit", seed=5)
     eng.step(a, 3, 1.0)
@@ -75,9 +81,10 @@ def test_ragged_launch_equals_solo_launches_bitwise():
                 assert torch.equal(u, v), x["name"]
 
 
-def test_two_runs_are_bitwise_identical():
+@pytest.mark.parametrize("path", ["fp32", "tc"])
+def test_two_runs_are_bitwise_identical(path):
     torch = need_gpu()
-    eng, w = engine()
+    eng, w = engine(path=path)
     shapes = [("a", (300, 700)), ("b", (700,)), ("c", (2048, 96))]
     a = make_states(shapes, recipe="vit", seed=6)
     b = make_states(shapes, recipe="vit", seed=6)
@@ -90,9 +97,10 @@ def test_two_runs_are_bitwise_identical():
         assert torch.equal(x["mom"][2], y["mom"][2])
 
 
-def test_misaligned_views_take_the_scalar_path():
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_misaligned_views_take_the_scalar_path(path, tol):
     torch = need_gpu()
-    eng, w = engine()
+    eng, w = engine(path=path)
     base = make_states([("w", (40, 64))], recipe="vit", seed=7)[0]
     st = {}
     n = base["rows"] * base["cols"]
@@ -106,7 +114,7 @@ def test_misaligned_views_take_the_scalar_path():
         buf[1:].copy_(m)
         st["mom"].append(buf[1:])
     st.update(row=base["row"], col=base["col"], rows=40, cols=64, weight_set=0, name="mis")
-    compare_step(eng, [st], w, 32, 1, 1.0, TOL_FP32)
+    compare_step(eng, [st], w, 32, 1, 1.0, tol)
 
 
 def test_validation_leaves_state_untouched():
@@ -151,7 +159,8 @@ def test_resume_from_saved_state_is_bitwise_identical():
         assert torch.equal(x["param"], y["param"])
 
 
-def test_identity_mlp_is_normalised_sgd_on_gpu():
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_identity_mlp_is_normalised_sgd_on_gpu(path, tol):
     """Closed form on the GPU: routing weights make the step normalised SGD."""
     torch = need_gpu()
     from learned_optimizer_step_gb300 import LearnedOptimizer
@@ -161,13 +170,13 @@ def test_identity_mlp_is_normalised_sgd_on_gpu():
     W3 = np.zeros((H, 2)); W3[0, 0] = 1.0; W3[1, 0] = -1.0
     wf = np.concatenate([W1.ravel(), np.zeros(H), W2.ravel(), np.zeros(H), W3.ravel(),
                          [0.0, 300.0]]).astype(np.float32)
-    eng = LearnedOptimizer(wf, H, "fp32")
+    eng = LearnedOptimizer(wf, H, path)
     st = make_states([("w", (128, 256))], recipe="vit", seed=10)[0]
     p0 = cpu(st["param"]); g = cpu(st["grad"])
     eng.step([st], 1, 0.25)
     torch.cuda.synchronize()
     expect = p0 - 0.25 * 1e-3 * np.exp(0.3) * g / np.sqrt(np.mean(g * g) + 1e-30)
-    assert rel_err(cpu(st["param"]), expect) < 1e-5
+    assert rel_err(cpu(st["param"]), expect) < tol
 
 
 def _sample(n_per=512, seed=0):
@@ -192,12 +201,13 @@ def _unique_shape_subset(states):
     return out
 
 
-def test_vit_b16_full_size_sampled():
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_vit_b16_full_size_sampled(path, tol):
     """Full ViT-B/16 list in one launch per kernel; every tensor's stats and
     accumulators are compared in full, parameters at sampled elements, for
     one tensor of each distinct shape."""
     torch = need_gpu()
-    eng, w = engine()
+    eng, w = engine(path=path)
     wl = synth.workloads()["vit_b16"]
     states = synth.make_list(wl, "cuda", seed=0)
     ref_states = _unique_shape_subset(states)
@@ -213,17 +223,18 @@ def test_vit_b16_full_size_sampled():
         r = ref[id(st)]
         sidx = pick(st)
         out = O.step_tensor(r, 1, 1.0, ws, sample_idx=sidx)
-        assert rel_err(cpu(st["param"])[sidx], out["sample_param"]) <= TOL_FP32, st["name"]
+        assert rel_err(cpu(st["param"])[sidx], out["sample_param"]) <= tol, st["name"]
         assert rel_err(eng.feature_stats(idx), out["S"], floor=1e-300) <= 2e-5, st["name"]
         assert rel_err(cpu(st["mom"][1]), r["mom"][1]) <= 2e-6
         assert rel_err(cpu(st["col"][0]), r["col"][0]) <= 2e-6, st["name"]
 
 
-def test_gpt2_heavy_tails_late_step_sampled():
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_gpt2_heavy_tails_late_step_sampled(path, tol):
     """GPT-2-small list, Student-t gradients, t = 9991 with warmed-up
     accumulators; checks the token embedding and one tensor per shape."""
     torch = need_gpu()
-    eng, w = engine()
+    eng, w = engine(path=path)
     wl = synth.workloads()["gpt2_small"]
     states = synth.make_list(wl, "cuda", seed=0)
     ref_states = _unique_shape_subset(states)
@@ -238,5 +249,5 @@ def test_gpt2_heavy_tails_late_step_sampled():
         r = ref[id(st)]
         sidx = pick(st)
         out = O.step_tensor(r, wl.first_step, 1.0, ws, sample_idx=sidx)
-        assert rel_err(cpu(st["param"])[sidx], out["sample_param"]) <= TOL_FP32, st["name"]
+        assert rel_err(cpu(st["param"])[sidx], out["sample_param"]) <= tol, st["name"]
         assert rel_err(eng.feature_stats(idx), out["S"], floor=1e-300) <= 2e-5, st["name"]
