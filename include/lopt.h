@@ -51,6 +51,7 @@ extern "C" {
 #define LOPT_E_UNSUPPORTED -6  /* hidden width / MLP path not available    */
 #define LOPT_E_TIMEOUT     -7  /* a bounded device-side wait gave up       */
 #define LOPT_E_ALIAS       -8  /* two tensor buffers overlap               */
+#define LOPT_E_TOO_LARGE   -9  /* needs more than the fixed static scratch */
 
 /* ---- fixed sizes ------------------------------------------------------- */
 #define LOPT_D_FEAT        39  /* 28 per-element + 11 time features        */
@@ -176,6 +177,41 @@ int lopt_set_kernel_timing(lopt_handle h, int enable);
  * timed step; resets the sums.
  */
 int lopt_kernel_times(lopt_handle h, double* ms, int64_t* launches);
+
+/*
+ * Row/column second-moment update of ONE tensor without any device
+ * allocation.  The paper has no counterpart to this entry point; it exists
+ * for callers that cannot call cudaMalloc: code running inside a runtime or
+ * framework that owns every device allocation, or under a fixed device-memory
+ * budget, or on a path where cudaMalloc's implicit device-wide
+ * synchronisation is not acceptable.  It runs the same row/column kernel as
+ * lopt_step() (same strips, same summation order) but takes its scratch from
+ * a fixed array of LOPT_STATIC_SCRATCH_BYTES bytes that the library reserves
+ * in device memory of every GPU on which it is loaded, held until the process
+ * exits.  No handle is needed.
+ *   grad     DEVICE [rows*cols] fp32, read.
+ *   row      HOST array of 3 DEVICE pointers, [rows] fp32 each: the row
+ *            accumulators (decays 0.1, 0.5, 0.9), updated in place.
+ *   col      HOST array of 3 DEVICE pointers, [cols] fp32 each: the column
+ *            accumulators, updated in place.
+ *   rows, cols  the [rows x cols] view, as in lopt_tensor.
+ *   inv_rho  DEVICE [3] fp32, written: 1 / mean_i row[k][i] after the
+ *            update, or 0 where that mean is 0.
+ *   stream   cudaStream_t (NULL = legacy default stream).
+ * Asynchronous on `stream`.  The first call on a device looks up that
+ * device's scratch address (once, with the device current); make that first
+ * call before any stream capture.  Every call on a device shares the one
+ * scratch array, which keeps the previous call's contents (the call clears
+ * the parts that must start at zero), so calls that overlap on the GPU --
+ * two streams, or two host threads -- race and must be ordered by the caller.
+ * Errors: LOPT_E_ARG / LOPT_E_ALIGN / LOPT_E_SHAPE / LOPT_E_ALIAS
+ * (validation, nothing enqueued), LOPT_E_TOO_LARGE (the tensor needs more
+ * than LOPT_STATIC_SCRATCH_BYTES of scratch; nothing enqueued),
+ * LOPT_E_CUDA.
+ */
+#define LOPT_STATIC_SCRATCH_BYTES (2u << 20)
+int lopt_rowcol_static(const float* grad, float* const* row, float* const* col,
+                       int64_t rows, int64_t cols, float* inv_rho, void* stream);
 
 /* Release every device allocation of the handle (waits for its work). */
 int lopt_destroy(lopt_handle h);

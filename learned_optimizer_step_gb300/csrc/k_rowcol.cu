@@ -15,6 +15,12 @@
 // rows, and writes per-strip column partial sums.  The last strip block of a
 // tensor (a per-tensor counter; no spin-waits) sums the column partials and
 // row partials in a fixed order, so results do not depend on block timing.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "lopt.h"
 #include "lopt_internal.cuh"
 
 namespace lopt {
@@ -205,3 +211,137 @@ cudaError_t launch_rowcol(const StepArgs& a, cudaStream_t s) {
 }
 
 }  // namespace lopt
+
+// ---- no-allocation entry point ----------------------------------------------
+// lopt_rowcol_static() runs the kernel above for one tensor with all of its
+// scratch (descriptor, unit table, per-tensor results, counter, column and
+// row partials) carved from one fixed array in device memory, so it never
+// calls cudaMalloc.  The array belongs to the library image: every GPU that
+// loads the library holds LOPT_STATIC_SCRATCH_BYTES for it until the process
+// exits, and all calls on a device share it.
+namespace lopt {
+namespace {
+
+__device__ __align__(256) unsigned char g_rowcol_scratch[LOPT_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxScratchDevices] = {};
+
+// Device address of the scratch array on the current device.  Host code may
+// not use the symbol itself (it names a host-side stand-in), so the address
+// is looked up once per device, with that device current, and cached.
+int scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return LOPT_E_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxScratchDevices) return LOPT_E_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_rowcol_scratch);
+    if (e != cudaSuccess || !p) {
+      cudaGetLastError();
+      return LOPT_E_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return LOPT_OK;
+}
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+}  // namespace
+}  // namespace lopt
+
+extern "C" int lopt_rowcol_static(const float* grad, float* const* row, float* const* col,
+                                  int64_t rows, int64_t cols, float* inv_rho, void* stream_ptr) {
+  using namespace lopt;
+  if (!grad || !row || !col || !inv_rho) return LOPT_E_ARG;
+  if (rows < 1 || cols < 1) return LOPT_E_SHAPE;
+  if (rows > ((int64_t)1 << 31) || cols > ((int64_t)1 << 31) || rows * cols >= ((int64_t)1 << 31))
+    return LOPT_E_SHAPE;
+  struct Span { uintptr_t lo, hi; };
+  std::vector<Span> spans = {{(uintptr_t)grad, (uintptr_t)grad + (uintptr_t)(rows * cols) * 4},
+                             {(uintptr_t)inv_rho, (uintptr_t)inv_rho + 12}};
+  for (int k = 0; k < 3; ++k) {
+    if (!row[k] || !col[k]) return LOPT_E_ARG;
+    spans.push_back({(uintptr_t)row[k], (uintptr_t)row[k] + (uintptr_t)rows * 4});
+    spans.push_back({(uintptr_t)col[k], (uintptr_t)col[k] + (uintptr_t)cols * 4});
+  }
+  for (const Span& sp : spans)
+    if (sp.lo % 4) return LOPT_E_ALIGN;
+  std::sort(spans.begin(), spans.end(), [](const Span& a, const Span& b) { return a.lo < b.lo; });
+  for (size_t k = 1; k < spans.size(); ++k)
+    if (spans[k].lo < spans[k - 1].hi) return LOPT_E_ALIAS;
+
+  // Same decomposition as lopt_step(), so the results are the same bits.
+  const int strip_rows = strip_rows_for(rows, cols);
+  const int n_strips = (int)((rows + strip_rows - 1) / strip_rows);
+  const size_t o_desc = 0;
+  const size_t o_units = o_desc + round256(sizeof(TensorDesc));
+  const size_t o_aux = o_units + round256(sizeof(Unit) * (size_t)n_strips);
+  const size_t o_cnt = o_aux + round256(sizeof(TensorAux));
+  const size_t o_row = o_cnt + 256;                       // counter + status
+  const size_t o_col = o_row + round256(sizeof(double) * 3 * (size_t)n_strips);
+  const size_t need = o_col + sizeof(float) * (size_t)n_strips * (size_t)cols;
+  if (need > LOPT_STATIC_SCRATCH_BYTES) return LOPT_E_TOO_LARGE;
+
+  void* base = nullptr;
+  int rc = scratch_address(&base);
+  if (rc != LOPT_OK) return rc;
+  char* sc = static_cast<char*>(base);
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+
+  TensorDesc d;
+  std::memset(&d, 0, sizeof(d));
+  d.g = grad;
+  for (int k = 0; k < 3; ++k) {
+    d.r[k] = row[k];
+    d.c[k] = col[k];
+  }
+  d.R = rows;
+  d.C = cols;
+  d.N = rows * cols;
+  bool v4 = ((uintptr_t)grad & 15) == 0;
+  for (int k = 0; k < 3; ++k) v4 = v4 && (((uintptr_t)col[k] & 15) == 0);
+  d.vec4 = v4 ? 1 : 0;
+  d.strip_rows = strip_rows;
+  d.n_strips = n_strips;
+  d.colpart_off = 0;
+  d.rowpart_off = 0;
+  std::vector<Unit> units((size_t)n_strips);
+  for (int s = 0; s < n_strips; ++s) units[(size_t)s] = {0, s};
+
+  // Pageable sources are staged by the runtime before these calls return.
+  cudaError_t e = cudaMemcpyAsync(sc + o_desc, &d, sizeof(d), cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(sc + o_units, units.data(), sizeof(Unit) * units.size(),
+                        cudaMemcpyHostToDevice, stream);
+  // The last-block counter and the status word must start at zero.
+  if (e == cudaSuccess) e = cudaMemsetAsync(sc + o_cnt, 0, 256, stream);
+  if (e == cudaSuccess) {
+    StepArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.desc = reinterpret_cast<const TensorDesc*>(sc + o_desc);
+    a.units = reinterpret_cast<const Unit*>(sc + o_units);
+    a.n_units = n_strips;
+    a.aux = reinterpret_cast<TensorAux*>(sc + o_aux);
+    a.counters = reinterpret_cast<int32_t*>(sc + o_cnt);
+    a.status = reinterpret_cast<int32_t*>(sc + o_cnt + 16);
+    a.rowpart = reinterpret_cast<double*>(sc + o_row);
+    a.colpart = reinterpret_cast<float*>(sc + o_col);
+    e = launch_rowcol(a, stream);
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(inv_rho, sc + o_aux + offsetof(TensorAux, inv_rho), 3 * sizeof(float),
+                        cudaMemcpyDeviceToDevice, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return LOPT_E_CUDA;
+  }
+  return LOPT_OK;
+}

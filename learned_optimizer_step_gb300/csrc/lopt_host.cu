@@ -22,7 +22,20 @@
 
 namespace lopt {
 bool apply_fp32_supported(int hidden);
+
+// Rows per K0 strip.  About kStripTarget elements per strip, but no more
+// than kFinalizeCap / cols strips (the last block of a tensor sums
+// strips x cols column partials) and no more than kMaxStripRows rows.
+int strip_rows_for(int64_t R, int64_t C) {
+  const int64_t N = R * C;
+  int64_t strips = std::max<int64_t>(1, (N + kStripTarget - 1) / kStripTarget);
+  strips = std::min<int64_t>(strips, std::max<int64_t>(1, kFinalizeCap / std::max<int64_t>(C, 1)));
+  strips = std::min<int64_t>(strips, R);
+  int64_t rows = (R + strips - 1) / strips;
+  rows = std::min<int64_t>(rows, kMaxStripRows);
+  return (int)std::max<int64_t>(rows, 1);
 }
+}  // namespace lopt
 
 using namespace lopt;
 
@@ -112,19 +125,6 @@ int validate(const lopt_ctx* h, const lopt_tensor* ts, int n) {
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
-
-// Rows per K0 strip.  About kStripTarget elements per strip, but no more
-// than kFinalizeCap / cols strips (the last block of a tensor sums
-// strips x cols column partials) and no more than kMaxStripRows rows.
-int strip_rows_for(int64_t R, int64_t C) {
-  const int64_t N = R * C;
-  int64_t strips = std::max<int64_t>(1, (N + kStripTarget - 1) / kStripTarget);
-  strips = std::min<int64_t>(strips, std::max<int64_t>(1, kFinalizeCap / std::max<int64_t>(C, 1)));
-  strips = std::min<int64_t>(strips, R);
-  int64_t rows = (R + strips - 1) / strips;
-  rows = std::min<int64_t>(rows, kMaxStripRows);
-  return (int)std::max<int64_t>(rows, 1);
-}
 
 int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t stream) {
   std::vector<TensorDesc> desc(n);
@@ -253,6 +253,7 @@ const char* lopt_strerror(int code) {
     case LOPT_E_UNSUPPORTED: return "unsupported configuration";
     case LOPT_E_TIMEOUT: return "device-side wait timed out";
     case LOPT_E_ALIAS: return "tensor buffers overlap";
+    case LOPT_E_TOO_LARGE: return "tensor needs more scratch than the static no-allocation buffer";
     default: return "unknown error";
   }
 }

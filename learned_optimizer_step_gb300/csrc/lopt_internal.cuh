@@ -172,6 +172,7 @@ enum : int32_t { kStatusTimeout = 1 };
 
 // ---- launchers (one per kernel file) ---------------------------------------
 cudaError_t launch_rowcol(const StepArgs& a, cudaStream_t s);
+int  strip_rows_for(int64_t R, int64_t C);   // K0 rows per strip of an [R x C] tensor
 cudaError_t launch_stats(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_apply_fp32(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_apply_tc(const StepArgs& a, cudaStream_t s);

@@ -28,11 +28,12 @@ _PATHS = {"fp32": MLP_FP32, "tc": MLP_TC}
 ERRORS = {
     -1: "LOPT_E_ARG", -2: "LOPT_E_SHAPE", -3: "LOPT_E_ALIGN", -4: "LOPT_E_CUDA",
     -5: "LOPT_E_OOM", -6: "LOPT_E_UNSUPPORTED", -7: "LOPT_E_TIMEOUT", -8: "LOPT_E_ALIAS",
+    -9: "LOPT_E_TOO_LARGE",
 }
 
 EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_step",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
-            "lopt_destroy", "lopt_strerror", "lopt_version")
+            "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_version")
 
 
 class LoptTensor(ctypes.Structure):
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_set_kernel_timing.restype = i32
     lib.lopt_kernel_times.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)]
     lib.lopt_kernel_times.restype = i32
+    lib.lopt_rowcol_static.argtypes = [vp, ctypes.POINTER(vp), ctypes.POINTER(vp), i64, i64, vp, vp]
+    lib.lopt_rowcol_static.restype = i32
     lib.lopt_destroy.argtypes = [vp]
     lib.lopt_destroy.restype = i32
     lib.lopt_strerror.argtypes = [i32]
@@ -235,3 +238,20 @@ def zeros_state(param, grad, rows: int, cols: int, weight_set: int = 0) -> Tenso
     return TensorState(param.reshape(-1), grad.reshape(-1), [z(n) for _ in range(3)], z(n),
                        [z(rows) for _ in range(3)], [z(cols) for _ in range(3)], rows, cols,
                        weight_set)
+
+
+def rowcol_static(grad, row, col, rows: int, cols: int, inv_rho, stream=None) -> None:
+    """Row/column second-moment update of one tensor through
+    lopt_rowcol_static(), which allocates no device memory (its scratch is a
+    fixed array inside the library).  For callers that may not call
+    cudaMalloc.  ``row``/``col``: three tensors each, updated in place;
+    ``inv_rho``: a 3-float tensor that receives 1 / mean(row[k])."""
+    import torch
+    rp = (ctypes.c_void_p * 3)(*[_ptr(r, rows, "row") for r in row])
+    cp = (ctypes.c_void_p * 3)(*[_ptr(c, cols, "col") for c in col])
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check("lopt_rowcol_static", load_library().lopt_rowcol_static(
+        _ptr(grad, rows * cols, "grad"), rp, cp, int(rows), int(cols), _ptr(inv_rho, 3, "inv_rho"),
+        ctypes.c_void_p(handle)))

@@ -76,6 +76,7 @@ def test_validation_before_any_device_call(lib):
     assert lib.lopt_feature_stats(None, 0, None) == -1
     assert lib.lopt_set_kernel_timing(None, 1) == -1
     assert lib.lopt_kernel_times(None, None, None) == -1
+    assert lib.lopt_rowcol_static(None, None, None, 4, 4, None, None) == -1
 
 
 def test_binding_rejects_non_cuda_tensors():
