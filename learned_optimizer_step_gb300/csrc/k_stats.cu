@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kT) k_stats(StepArgs a) {
     for (int x = 0; x < d.k1_units; ++x) s += (double)__ldcg(part + (int64_t)x * kStats + tid);
     a.aux[u.tensor].S[tid] = s;
     scale[tid] = 1.0 / sqrt(s / (double)d.N + 1e-30);
+    a.aux[u.tensor].scale[tid] = (float)scale[tid];
   }
   __syncthreads();
 
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kT) k_stats(StepArgs a) {
       out[kStats * H + h] = (float)b;
     }
   } else {
-    fold_w1_tc(H, W1, b1, scale, a.t, out);
+    fold_w1_tc(H, W1, b1, a.t, out);
   }
   if (tid == 0) a.counters[u.tensor] = 0;
 }

@@ -72,6 +72,7 @@ struct TensorAux {
   float  inv_rho[3];     // 1 / mean_i r_k[i], or 0 when that mean is 0
   float  pad0;
   double S[kStats];      // sum over elements of feature^2
+  float  scale[kStats];  // 1 / sqrt(S / N + eps): the normalisation factors
 };
 
 // Everything a launch needs, passed by value.

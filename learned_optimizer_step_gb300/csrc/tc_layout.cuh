@@ -1,15 +1,16 @@
 // Tensor-core (tcgen05) helpers and operand layouts of the apply pass.
 //
 // The per-element MLP is evaluated as three batched GEMMs over a tile of 128
-// elements (one element per TMEM lane / accumulator row):
-//   layer 1  [128 x 32] (28 features, a constant-1 bias column, 3 zeros, TF32)
-//            x [32 x NP] (folded W1 and b1, TF32)
-//   layer 2  [128 x K2] (ReLU(h1) as FP16, a constant-1 column, zeros)
-//            x [K2 x NP] (W2 and b2, FP16)
-//   layer 3  [128 x K2] (ReLU(h2) as FP16, constant-1, zeros)
-//            x [K2 x 16] (W3 and b3 in the first two columns, FP16)
-// NP = hidden width padded to a multiple of 16 (>= 16), K2 = NP + 1 padded to
-// a multiple of 16.  Accumulation is FP32 in tensor memory.
+// elements (one element per TMEM lane / accumulator row), all kind::f16 with
+// FP32 accumulation in tensor memory:
+//   layer 1  [128 x 32]  normalised features 0..27, a constant-1 column, 3
+//                        zeros (FP16)  x  [32 x NP]  W1 rows 0..27 and the
+//                        bias b1 + sum_s tau_s W1[28 + s] (FP16)
+//   layer 2  [128 x NP]  ReLU(h1) (FP16)  x  [NP x NP] W2 (FP16), added to an
+//                        accumulator preset to b2
+//   layer 3  [128 x NP]  ReLU(h2) (FP16)  x  [NP x 16] W3 in columns 0, 1;
+//                        b3 is added afterwards
+// NP = hidden width padded to 16 or 32.
 //
 // Operands live in shared memory in the canonical K-major layout without
 // swizzle: 8-row x 16-byte core matrices, core matrices adjacent along K 128
@@ -17,18 +18,17 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
+
 #include "lopt_internal.cuh"
 
 namespace lopt {
 
 __host__ __device__ constexpr int tc_np(int hp) { return hp < 16 ? 16 : (hp + 15) / 16 * 16; }
-__host__ __device__ constexpr int tc_k2(int np) { return (np + 1 + 15) / 16 * 16; }
 
-// Element offsets inside one canonical operand (row r of the M/N side, k on K).
-__host__ __device__ constexpr int tf32_off(int r, int k) {         // K = 32, 4-byte elements
-  return (r >> 3) * 256 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3);
-}
-__host__ __device__ constexpr int f16_off(int r, int k, int K) {   // 2-byte elements
+// Element offset inside one canonical FP16 operand with K columns (row r of
+// the M/N side, column k).
+__host__ __device__ constexpr int f16_off(int r, int k, int K) {
   return (r >> 3) * (K * 8) + (k >> 3) * 64 + (r & 7) * 8 + (k & 7);
 }
 
@@ -127,6 +127,36 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+         "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+         "r"(r[14]), "r"(r[15]) : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+         "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+         "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+         "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+         "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31]) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Round-to-nearest FP16 of two floats, packed (lo = a, hi = b).
+__device__ __forceinline__ uint32_t f16x2(float a, float b) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+  return d;
+}
+
 __device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
                : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
@@ -179,25 +209,62 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-// Fold the per-tensor normalisation and the time features into layer 1 and
-// store it as the canonical TF32 B operand [NP x 32]:
-//   B[n][k] = s_k * W1[k][n] (k < 28),  b1[n] + sum_s tau_s W1[28+s][n] (k = 28),
+// Plain arrive (count 1) and arrive that also expects `tx` transaction bytes.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(smem_u32(bar)), "r"(tx)
+               : "memory");
+}
+
+// Bulk copy global -> shared (own CTA), completion counted on `bar` in bytes.
+// Both addresses 16-byte aligned, `bytes` a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+// Wait for phase `parity` of `bar`, at most `limit_ns`; gives up early when
+// *abort becomes non-zero.  On its own timeout it sets *abort.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                   volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) == 0) {
+      if (*abort) return false;
+      if (global_ns() - t0 > limit_ns) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+  *abort = 1;
+  return false;
+}
+
+// Layer-1 B operand [NP x 32] (FP16) for the tensor-core path:
+//   B[n][k] = W1[k][n] (k < 28),  b1[n] + sum_s tau_s W1[28+s][n] (k = 28),
 //   0 otherwise or for padded units n >= hp.
-__device__ inline void fold_w1_tc(int hp, const float* W1, const float* b1, const double* scale,
-                                  double t, float* out) {
+// (The normalisation scales are applied to the features themselves.)
+__device__ inline void fold_w1_tc(int hp, const float* W1, const float* b1, double t, float* out) {
   const int np = tc_np(hp);
+  __half* o = reinterpret_cast<__half*>(out);
   for (int x = threadIdx.x; x < np * 32; x += blockDim.x) {
     const int n = x >> 5, k = x & 31;
     double v = 0.0;
     if (n < hp) {
       if (k < kStats) {
-        v = scale[k] * (double)W1[k * hp + n];
+        v = (double)W1[k * hp + n];
       } else if (k == kStats) {
         v = (double)b1[n];
         for (int s = 0; s < kTimeFeat; ++s) v += tanh(t / time_scale(s)) * (double)W1[(kStats + s) * hp + n];
       }
     }
-    out[tf32_off(n, k)] = tf32_round((float)v);
+    o[f16_off(n, k, 32)] = __float2half_rn((float)v);
   }
 }
 
