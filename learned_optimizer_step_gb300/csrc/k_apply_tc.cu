@@ -9,27 +9,34 @@
 // 44 bytes of traffic).
 //
 // One persistent CTA per SM, warp-specialised, linked by mbarriers:
-//   warp 16      producer: bulk-copies (cp.async.bulk) p, g, m0..2, v of the
-//                next tiles into a ring of shared-memory stages;
+//   warp 16      producer: bulk-copies (cp.async.bulk, one array per lane) p,
+//                g, m0..2, v of the next 8 tiles of a work unit into a ring
+//                of shared-memory stages;
 //   warps 8-15   two feature warpgroups (alternate tiles): EMA update,
-//                features, normalisation, FP16 A tile of layer 1 into a tile
-//                slot; they also store the updated accumulators m and v;
+//                features, normalisation, FP16 A operand of layer 1 into the
+//                tile slot's tensor memory; they also store the updated
+//                accumulators m and v;
 //   warp 17      MMA issuer (one thread);
-//   warps 0-7    two epilogue warpgroups (alternate tiles; tensor-memory
-//                lanes 0-127): ReLU + FP16 A tiles of layers 2 and 3, the
-//                b2 preset of the layer-2 accumulator, and the update of p.
-// A tile is 128 consecutive elements of one tensor (one per TMEM lane).
+//   warps 0-7    two epilogue warpgroups (alternate tiles): ReLU + FP16 A
+//                operand of layer 2 (in tensor memory) and the b2 preset of
+//                its accumulator; then ReLU(h2), the two-unit output layer in
+//                FP32 on the CUDA cores, and the update of p.
+// A tile is 128 consecutive elements of one tensor (one per TMEM lane).  A
+// tile slot is a set of tensor-memory columns: the FP32 accumulator (NP
+// columns) and the FP16 A operand of the next MMA (16 columns); the A
+// operands never pass through shared memory.
 //
-// Small MMAs (M=128, N<=32) cost about 40 cycles of the SM's MMA pipe each,
-// whatever their K, so a tile uses as few as possible: FP16 operands with
-// K = 32 for layer 1 (2 MMAs) and K = NP for layers 2 and 3 (2 MMAs each at
-// NP = 32), biases without extra K columns, and one tcgen05.commit per
-// issue iteration.  Stages of different tiles overlap with fixed lags: in
-// iteration k the MMA thread issues layer 1 of tile k, layer 2 of tile k-5
-// and layer 3 of tile k-11 (K-steps interleaved), then commits once; in step
-// m an epilogue group finishes layer 1 of tile m-2, layer 2 of tile m-8 and
-// the update of tile m-14.  No role waits on work issued in the same
-// iteration, and at most 15 tiles are in flight (16 slots).
+// Small MMAs (M=128, N<=32) cost about 40-50 cycles of the SM's MMA pipe
+// each, whatever their K, and an MMA's result reaches a waiting thread about
+// a thousand cycles after issue.  So a tile uses few MMAs (FP16 operands,
+// K = 32 for layer 1 and K = NP for layer 2: 4 MMAs at NP = 32, biases
+// without extra K columns, one tcgen05.commit per issue iteration) and only
+// two MMA round trips: the output layer (two units) runs on the CUDA cores.
+// Stages of different tiles overlap with fixed lags chosen for the largest
+// slack around that latency: in iteration k the MMA thread issues layer 1 of
+// tile k and layer 2 of tile k-5 (K-steps interleaved), then commits once;
+// in step m an epilogue group finishes layer 1 of tile m-4 and the rest of
+// tile m-8.  At most 9 tiles are in flight (10 slots at NP = 32).
 //
 // The tiles of a CTA are processed in sessions: maximal runs of tiles whose
 // tensors share one MLP weight set.  Between sessions the pipeline drains,
@@ -49,38 +56,38 @@ namespace {
 
 constexpr int kTile = 128;                // elements per tile (= TMEM lanes)
 constexpr int kThreads = 18 * 32;         // 8 epilogue + 8 feature + producer + MMA warps
-constexpr int kSlots = 16;                // tiles in flight
-constexpr int kRingStages = 20;           // input stages (one tile each)
-constexpr int kStageBytes = 6 * kTile * 4;
+constexpr int kStageTiles = 8;            // tiles per input stage (4 KB per array)
+constexpr int kStageElems = kStageTiles * kTile;
+constexpr int kRingStages = 5;            // input stages
+constexpr int kStageBytes = 6 * kStageElems * 4;
 constexpr int kDone = 8;                  // commit barriers (one per MMA iteration)
-constexpr int kLag2 = 5, kLag3 = 11;      // MMA: layer 2 / 3 of tiles k-5 / k-11
-constexpr int kE1 = 2, kE2 = 8, kE3 = 14; // epilogue step m: tiles m-2, m-8, m-14
+constexpr int kLag2 = 5;                  // MMA iteration k: layer 2 of tile k-5
+constexpr int kE1 = 4, kE2 = 8;           // epilogue step m: tiles m-4, m-8
 constexpr int kProducerWarp = 16, kMmaWarp = 17;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 template <int NP>
 struct Geom {
-  static constexpr int Slot = kTile * 32 * 2;          // 8 KB: largest A tile (layer 1)
-  static constexpr int SBO1 = 32 * 16;                 // layer-1 operands: K = 32
-  static constexpr int SBO = NP * 16;                  // layer-2/3 operands: K = NP
+  static constexpr int ACols = 16;                     // A operand: 32 FP16 per row
+  static constexpr int SlotCols = NP + ACols;          // accumulator + A operand
+  static constexpr int S = 512 / SlotCols < 16 ? 512 / SlotCols : 16;   // tiles in flight
+  static constexpr int SBO1 = 32 * 16;                 // layer-1 B operand: K = 32
+  static constexpr int SBO = NP * 16;                  // layer-2/3 B operands: K = NP
   static constexpr int B1 = NP * 32 * 2;
   static constexpr int B2 = NP * NP * 2;
-  static constexpr int B3 = 16 * NP * 2;
-  static constexpr int Bias = (NP + 4) * 4;            // b2[NP], b3[2], pad
-  static constexpr int Set = (B2 + B3 + Bias + 1023) / 1024 * 1024;   // packed per-set stride
-  static constexpr int oSlots = 0;
-  static constexpr int oRing = kSlots * Slot;
+  static constexpr int Aux = (3 * NP + 4) * 4;         // b2[NP], W3 pairs[NP][2], b3[2], pad
+  static constexpr int Set = (B2 + Aux + 1023) / 1024 * 1024;   // packed per-set stride
+  static constexpr int oRing = 0;
   static constexpr int oB1 = oRing + kRingStages * kStageBytes;
-  static constexpr int oB2 = oB1 + B1;                  // B2, B3, b2, b3 as packed
+  static constexpr int oB2 = oB1 + B1;                  // B2, b2, W3, b3 as packed
   static constexpr int oBar = (oB2 + Set + 15) / 16 * 16;
-  static constexpr int nBars = 2 * kRingStages + 4 * kSlots + kDone;
+  static constexpr int nBars = 2 * kRingStages + 3 * S + kDone;
   static constexpr int oInfo = oBar + nBars * 8;
   static constexpr int Smem = oInfo + 64;
-  static constexpr int TmemCols = kSlots * NP <= 256 ? 256 : 512;
+  static constexpr int TmemCols = 512;
   static constexpr uint32_t ID12 = instr_desc(0, 128, NP);
-  static constexpr uint32_t ID3 = instr_desc(0, 128, 16);
   static_assert(Smem <= 232448, "shared memory of one CTA");
-  static_assert(kSlots * NP <= 512, "tensor memory columns");
+  static_assert(S * SlotCols <= 512 && S > kE2, "tensor memory columns / pipeline depth");
 };
 
 // Walks tiles in order: units [u, u1), 128-element tiles each.
@@ -89,7 +96,7 @@ struct TileWalk {
   const TensorDesc* desc;
   int64_t u, u1;
   int tensor;
-  int64_t start, end;
+  int64_t ustart, start, end;   // unit start, tile start, unit end
   __device__ void init(const Unit* un, const TensorDesc* de, int64_t b, int64_t e) {
     units = un; desc = de; u = b; u1 = e;
     load();
@@ -98,7 +105,7 @@ struct TileWalk {
     if (u < u1) {
       const Unit x = units[u];
       tensor = x.tensor;
-      start = (int64_t)x.local * kApplyChunk;
+      ustart = start = (int64_t)x.local * kApplyChunk;
       end = min(desc[tensor].N, start + (int64_t)kApplyChunk);
     }
   }
@@ -125,16 +132,13 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-// One FP16 A-operand row of layer 2 or 3: ReLU(h) in columns 0..NP-1.
+// ReLU + FP16 of one accumulator row, packed two per 32-bit column (16
+// columns: the A operand of the next layer, zero-padded past NP).
 template <int NP>
-__device__ __forceinline__ void store_h_row(uint32_t slot_addr, int row, const uint32_t* h) {
-  const uint32_t base = slot_addr + (row >> 3) * Geom<NP>::SBO + (row & 7) * 16;
+__device__ __forceinline__ void pack_relu_row(const uint32_t (&h)[NP], uint32_t (&av)[16]) {
 #pragma unroll
-  for (int kc = 0; kc < NP / 8; ++kc) {
-    const float* f = reinterpret_cast<const float*>(h + 8 * kc);
-    st_shared_v4(base + kc * 128, relu_f16x2(f[0], f[1]), relu_f16x2(f[2], f[3]),
-                 relu_f16x2(f[4], f[5]), relu_f16x2(f[6], f[7]));
-  }
+  for (int q = 0; q < 16; ++q)
+    av[q] = 2 * q < NP ? relu_f16x2(__uint_as_float(h[2 * q]), __uint_as_float(h[2 * q + 1])) : 0u;
 }
 
 template <int NP>
@@ -152,15 +156,14 @@ template <int NP>
 __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   static_assert(NP == 16 || NP == 32, "tensor-core path: padded hidden width 16 or 32");
   using G = Geom<NP>;
-  constexpr int S = kSlots, R = kRingStages;
+  constexpr int S = G::S, R = kRingStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   float* ring = reinterpret_cast<float*>(smem + G::oRing);
   uint64_t* ring_full = reinterpret_cast<uint64_t*>(smem + G::oBar);
   uint64_t* ring_empty = ring_full + R;
   uint64_t* a1_full = ring_empty + R;
   uint64_t* a2_full = a1_full + S;
-  uint64_t* a3_full = a2_full + S;
-  uint64_t* slot_empty = a3_full + S;
+  uint64_t* slot_empty = a2_full + S;
   uint64_t* done = slot_empty + S;
   int64_t* info = reinterpret_cast<int64_t*>(smem + G::oInfo);   // session: end unit, tiles
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::oInfo + 32);
@@ -190,12 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       info[1] = K;
       for (int r = 0; r < R; ++r) {
         mbar_init(ring_full + r, 1);
-        mbar_init(ring_empty + r, kTile);
+        mbar_init(ring_empty + r, 2 * kTile);   // every feature thread, once per stage
       }
       for (int s = 0; s < S; ++s) {
         mbar_init(a1_full + s, kTile);
         mbar_init(a2_full + s, kTile);
-        mbar_init(a3_full + s, kTile);
         mbar_init(slot_empty + s, kTile);
       }
       for (int s = 0; s < kDone; ++s) mbar_init(done + s, 1);
@@ -217,37 +219,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
 
     if (warp == kProducerWarp) {
       // ------------------------------ producer -------------------------------
-      if (lane == 0) {
-        TileWalk w;
-        w.init(a.units, a.desc, u0, u1);
-        int64_t k = 0;
-        for (; k < K; ++k, w.next()) {
-          const int st = (int)(k % R);
-          if (!mbar_wait_or_abort(ring_empty + st, (uint32_t)((k / R) & 1) ^ 1u, kWaitNs, abort_flag)) break;
-          const TensorDesc& d = a.desc[w.tensor];
-          if (d.vec4 && (d.C % 4 == 0)) {
-            const uint32_t bytes = (uint32_t)(min((int64_t)kTile, w.end - w.start) * 4);
-            mbar_arrive_expect_tx(ring_full + st, 6 * bytes);
-            float* dst = ring + st * (6 * kTile);
-            bulk_g2s(dst + 0 * kTile, d.p + w.start, bytes, ring_full + st);
-            bulk_g2s(dst + 1 * kTile, d.g + w.start, bytes, ring_full + st);
-            bulk_g2s(dst + 2 * kTile, d.m[0] + w.start, bytes, ring_full + st);
-            bulk_g2s(dst + 3 * kTile, d.m[1] + w.start, bytes, ring_full + st);
-            bulk_g2s(dst + 4 * kTile, d.m[2] + w.start, bytes, ring_full + st);
-            bulk_g2s(dst + 5 * kTile, d.v + w.start, bytes, ring_full + st);
-          } else {
-            mbar_arrive(ring_full + st);   // feature warps read global memory directly
+      // A stage holds up to 8 consecutive tiles of one work unit; lane q < 6
+      // copies array q of the stage.
+      int64_t n_st = 0;
+      for (int64_t u = u0; u < u1 && !*abort_flag; ++u) {
+        const Unit x = a.units[u];
+        const TensorDesc& d = a.desc[x.tensor];
+        const bool vec = d.vec4 && (d.C % 4 == 0);
+        const int64_t ue = min(d.N, (int64_t)x.local * kApplyChunk + kApplyChunk);
+        const float* src = lane == 0 ? d.p : lane == 1 ? d.g : lane == 2 ? d.m[0] : lane == 3 ? d.m[1]
+                         : lane == 4 ? d.m[2] : d.v;
+        bool stop = false;
+        for (int64_t e0 = (int64_t)x.local * kApplyChunk; e0 < ue; e0 += kStageElems, ++n_st) {
+          const int st = (int)(n_st % R);
+          if (!mbar_wait_or_abort(ring_empty + st, (uint32_t)((n_st / R) & 1) ^ 1u, kWaitNs, abort_flag)) {
+            stop = true;
+            break;
           }
+          const uint32_t bytes = (uint32_t)(min((int64_t)kStageElems, ue - e0) * 4);
+          if (lane == 0) {
+            if (vec) mbar_arrive_expect_tx(ring_full + st, 6 * bytes);
+            else mbar_arrive(ring_full + st);   // feature warps read global memory directly
+          }
+          __syncwarp();
+          if (vec && lane < 6) bulk_g2s(ring + st * (6 * kStageElems) + lane * kStageElems, src + e0, bytes,
+                                        ring_full + st);
         }
-        if (*abort_flag) {   // let copies already issued land before teardown
-          for (int64_t kk = (k > R ? k - R : 0); kk < k; ++kk)
-            mbar_drain(ring_full + kk % R, (uint32_t)((kk / R) & 1), kWaitNs / 10);
-        }
+        if (stop) break;
+      }
+      if (*abort_flag) {   // let copies already issued land before teardown
+        for (int64_t kk = (n_st > R ? n_st - R : 0); kk < n_st; ++kk)
+          mbar_drain(ring_full + kk % R, (uint32_t)((kk / R) & 1), kWaitNs / 10);
       }
     } else if (warp >= 8 && warp < 16) {
       // --------------------------- feature warpgroups ------------------------
       const int grp = (warp - 8) >> 2;
       const int t = tid - 256 - 128 * grp;
+      const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
       TileWalk w;
       w.init(a.units, a.desc, u0, u1);
       int cur = -1;
@@ -257,11 +265,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       float sc[kStats];
 #pragma unroll
       for (int q = 0; q < kStats; ++q) sc[q] = 0.f;
-      for (int64_t k = 0; k < K; ++k, w.next()) {
+      // input stage of the current tile: counter, ring index, offset in it
+      int64_t n_st = -1;
+      int st = 0, st_off = 0;
+      int64_t k = 0;
+      for (; k < K; ++k, w.next()) {
+        const int64_t in_unit = w.start - w.ustart;
+        if (in_unit % kStageElems == 0) {   // this tile opens a new stage
+          if (n_st >= 0) mbar_arrive(ring_empty + st);   // done with the previous one
+          ++n_st;
+          st = (int)(n_st % R);
+        }
+        st_off = (int)(in_unit % kStageElems);
         if ((int)(k & 1) != grp) continue;
-        const int s = (int)(k % S), st = (int)(k % R);
+        const int s = (int)(k % S);
         if (!mbar_wait_or_abort(slot_empty + s, (uint32_t)((k / S) & 1) ^ 1u, kWaitNs, abort_flag)) break;
-        if (!mbar_wait_or_abort(ring_full + st, (uint32_t)((k / R) & 1), kWaitNs, abort_flag)) break;
+        if (!mbar_wait_or_abort(ring_full + st, (uint32_t)((n_st / R) & 1), kWaitNs, abort_flag)) break;
         const TensorDesc& d = a.desc[w.tensor];
         if (w.tensor != cur) {
           cur = w.tensor;
@@ -278,17 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
         const bool valid = e < w.end;
         float p = 0.f, g = 0.f, m[3] = {0.f, 0.f, 0.f}, v = 0.f;
         if (vec) {
-          const float* rs = ring + st * (6 * kTile);
+          const float* rs = ring + st * (6 * kStageElems) + st_off + t;
           if (valid) {
-            p = rs[t]; g = rs[kTile + t]; m[0] = rs[2 * kTile + t]; m[1] = rs[3 * kTile + t];
-            m[2] = rs[4 * kTile + t]; v = rs[5 * kTile + t];
+            p = rs[0]; g = rs[kStageElems]; m[0] = rs[2 * kStageElems]; m[1] = rs[3 * kStageElems];
+            m[2] = rs[4 * kStageElems]; v = rs[5 * kStageElems];
           }
         } else if (valid) {
           p = __ldg(d.p + e); g = __ldg(d.g + e); v = __ldg(d.v + e);
 #pragma unroll
           for (int q = 0; q < 3; ++q) m[q] = __ldg(d.m[q] + e);
         }
-        mbar_arrive(ring_empty + st);
         float c[3] = {0.f, 0.f, 0.f};
         RowTerms rt;
 #pragma unroll
@@ -315,53 +333,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
           d.v[e] = v;
         }
-        // normalised features, FP16, into row t of the slot (K = 32)
-        const uint32_t row = s_base + G::oSlots + s * G::Slot + (t >> 3) * G::SBO1 + (t & 7) * 16;
+        // normalised features, FP16, into this lane's row of the slot's A
+        // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
+        uint32_t av[16];
 #pragma unroll
-        for (int kc = 0; kc < 3; ++kc) {
-          const int b = 8 * kc;
-          st_shared_v4(row + kc * 128, f16x2(f[b] * sc[b], f[b + 1] * sc[b + 1]),
-                       f16x2(f[b + 2] * sc[b + 2], f[b + 3] * sc[b + 3]),
-                       f16x2(f[b + 4] * sc[b + 4], f[b + 5] * sc[b + 5]),
-                       f16x2(f[b + 6] * sc[b + 6], f[b + 7] * sc[b + 7]));
-        }
-        st_shared_v4(row + 3 * 128, f16x2(f[24] * sc[24], f[25] * sc[25]),
-                     f16x2(f[26] * sc[26], f[27] * sc[27]), 0x00003C00u /* 1.0h, 0 */, 0u);
-        fence_proxy_async();
+        for (int q = 0; q < 14; ++q) av[q] = f16x2(f[2 * q] * sc[2 * q], f[2 * q + 1] * sc[2 * q + 1]);
+        av[14] = 0x00003C00u;   // 1.0h, 0
+        av[15] = 0u;
+        tmem_st16(t_lane + s * G::SlotCols + NP, av);
+        tmem_wait_st();
+        tc_fence_before();
         mbar_arrive(a1_full + s);
       }
+      if (k == K && n_st >= 0) mbar_arrive(ring_empty + st);
     } else if (warp == kMmaWarp) {
       // ------------------------------- MMA issuer ----------------------------
       if (lane == 0) {
-        const uint32_t s_slots = s_base + G::oSlots;
         const uint64_t dB1 = smem_desc(s_base + G::oB1, 128, G::SBO1);
         const uint64_t dB2 = smem_desc(s_base + G::oB2, 128, G::SBO);
-        const uint64_t dB3 = smem_desc(s_base + G::oB2 + G::B2, 128, G::SBO);
-        int64_t k = 0;
-        for (; k < K + kLag3; ++k) {
-          if (*abort_flag) break;
-          const bool do1 = k < K;
-          const bool do2 = k >= kLag2 && k - kLag2 < K;
-          const bool do3 = k >= kLag3 && k - kLag3 < K;
-          const int64_t k2 = k - kLag2, k3 = k - kLag3;
-          const int s1 = (int)(k % S), s2 = do2 ? (int)(k2 % S) : 0, s3 = do3 ? (int)(k3 % S) : 0;
-          if (do1 && !mbar_wait_or_abort(a1_full + s1, (uint32_t)((k / S) & 1), kWaitNs, abort_flag)) break;
-          if (do2 && !mbar_wait_or_abort(a2_full + s2, (uint32_t)((k2 / S) & 1), kWaitNs, abort_flag)) break;
-          if (do3 && !mbar_wait_or_abort(a3_full + s3, (uint32_t)((k3 / S) & 1), kWaitNs, abort_flag)) break;
+        const int k_end = (int)K + kLag2;
+        // slot index and phase of tile k and of tile k - kLag2, kept incrementally
+        int s1 = 0, s2 = S - kLag2;
+        uint32_t p1 = 0, p2 = 1;
+        int k = 0;
+        for (; k < k_end; ++k) {
+          const bool do1 = k < (int)K;
+          const bool do2 = k >= kLag2;
+          if (do1 && !mbar_wait_or_abort(a1_full + s1, p1, kWaitNs, abort_flag)) break;
+          if (do2 && !mbar_wait_or_abort(a2_full + s2, p2, kWaitNs, abort_flag)) break;
           tc_fence_after();
-          const uint64_t dA1 = smem_desc(s_slots + s1 * G::Slot, 128, G::SBO1);
-          const uint64_t dA2 = smem_desc(s_slots + s2 * G::Slot, 128, G::SBO);
-          const uint64_t dA3 = smem_desc(s_slots + s3 * G::Slot, 128, G::SBO);
-          // K-steps of the three layers interleaved (independent accumulators)
+          const uint32_t d1 = tmem + s1 * G::SlotCols, d2 = tmem + s2 * G::SlotCols;
+          // K-steps of the two layers interleaved (independent accumulators);
+          // one K-step of 16 FP16 values = 8 tensor-memory columns of A
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
-            if (do1) mma_f16(tmem + s1 * NP, dA1 + 16 * kk, dB1 + 16 * kk, G::ID12, kk > 0);
-            if (kk < NP / 16) {
-              if (do2) mma_f16(tmem + s2 * NP, dA2 + 16 * kk, dB2 + 16 * kk, G::ID12, 1u);   // onto b2
-              if (do3) mma_f16(tmem + s3 * NP, dA3 + 16 * kk, dB3 + 16 * kk, G::ID3, kk > 0);
-            }
+            if (do1) mma_f16_ts(d1, d1 + NP + 8 * kk, dB1 + 16 * kk, G::ID12, kk > 0);
+            if (do2 && kk < NP / 16) mma_f16_ts(d2, d2 + NP + 8 * kk, dB2 + 16 * kk, G::ID12, 1u);  // onto b2
           }
           mma_commit(done + (k % kDone));   // tracks every MMA issued so far
+          if (++s1 == S) { s1 = 0; p1 ^= 1; }
+          if (++s2 == S) { s2 = 0; p2 ^= 1; }
         }
         // nothing of ours may still be running when the session ends
         if (k > 0) mbar_drain(done + ((k - 1) % kDone), (uint32_t)(((k - 1) / kDone) & 1), kWaitNs / 10);
@@ -369,27 +380,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
     } else if (warp < 8) {
       // ------------------------------ epilogue -------------------------------
       // Group h takes the tiles k with k % 2 == h.  In step m it finishes
-      // layer 1 of tile m-2 (and presets the layer-2 accumulator to b2),
-      // layer 2 of tile m-8 and the update of tile m-14; it loads p of tile
-      // m-12 for the update two steps later.
+      // layer 1 of tile m-4 (ReLU, FP16 A operand of layer 2, b2 preset of
+      // its accumulator) and the rest of tile m-8 (ReLU(h2), output layer,
+      // update); it loads p of tile m-6 for the update two steps later.
       const int h = warp >> 2;
       const int t = tid - 128 * h;
       const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      const uint32_t s_slots = s_base + G::oSlots;
-      const float* bias = reinterpret_cast<const float*>(smem + G::oB2 + G::B2 + G::B3);
-      uint32_t b2[NP];
-#pragma unroll
-      for (int q = 0; q < NP; ++q) b2[q] = __float_as_uint(bias[q]);
-      const float b30 = bias[NP], b31 = bias[NP + 1];
-      TileWalk wp;   // tile m-12 of this group
+      const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
+      const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
+      const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
+      TileWalk wp;   // tile m-6 of this group
       wp.init(a.units, a.desc, u0, u1);
       if (h == 1) wp.next();
       const float lr = a.lr;
       float* p_ptr_prev = nullptr;
       float p_prev = 0.f;
-      for (int64_t m = h; m - kE3 < K; m += 2) {
+      for (int64_t m = h; m - kE2 < K; m += 2) {
         if (*abort_flag) break;
-        const int64_t t1 = m - kE1, t2 = m - kE2, t3 = m - kE3, tp = m - (kE3 - 2);
+        const int64_t t1 = m - kE1, t2 = m - kE2, tp = m - (kE2 - 2);
         float* p_ptr_next = nullptr;
         float p_next = 0.f;
         if (tp >= 0 && tp < K) {
@@ -405,13 +413,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           const int s = (int)(t1 % S);
           if (!mbar_wait_or_abort(done + (t1 % kDone), (uint32_t)((t1 / kDone) & 1), kWaitNs, abort_flag)) break;
           tc_fence_after();
-          uint32_t hv[NP];
-          tmem_ld_row<NP>(t_lane + s * NP, hv);
+          const uint32_t col = t_lane + s * G::SlotCols;
+          uint32_t hv[NP], av[16], b2[NP];
+          tmem_ld_row<NP>(col, hv);
+#pragma unroll
+          for (int q = 0; q < NP; q += 4) {
+            const float4 b = *reinterpret_cast<const float4*>(aux + q);
+            b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
+            b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
+          }
           tmem_wait_ld();
-          store_h_row<NP>(s_slots + s * G::Slot, t, hv);
-          tmem_st_row<NP>(t_lane + s * NP, b2);
+          pack_relu_row<NP>(hv, av);
+          tmem_st16(col + NP, av);
+          tmem_st_row<NP>(col, b2);
           tmem_wait_st();
-          fence_proxy_async();
           tc_fence_before();
           mbar_arrive(a2_full + s);
         }
@@ -421,28 +436,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           if (!mbar_wait_or_abort(done + (it % kDone), (uint32_t)((it / kDone) & 1), kWaitNs, abort_flag)) break;
           tc_fence_after();
           uint32_t hv[NP];
-          tmem_ld_row<NP>(t_lane + s * NP, hv);
+          tmem_ld_row<NP>(t_lane + s * G::SlotCols, hv);
           tmem_wait_ld();
-          store_h_row<NP>(s_slots + s * G::Slot, t, hv);
-          fence_proxy_async();
           tc_fence_before();
-          mbar_arrive(a3_full + s);
-        }
-        if (t3 >= 0 && t3 < K) {
-          const int s = (int)(t3 % S);
-          const int64_t it = t3 + kLag3;
-          if (!mbar_wait_or_abort(done + (it % kDone), (uint32_t)((it / kDone) & 1), kWaitNs, abort_flag)) break;
-          tc_fence_after();
-          uint32_t o[2];
-          tmem_ld2(t_lane + s * NP, o);
-          tmem_wait_ld();
+          mbar_arrive(slot_empty + s);   // the slot's tensor memory is no longer read
           if (p_ptr_prev) {
-            const float o0 = __uint_as_float(o[0]) + b30, o1 = __uint_as_float(o[1]) + b31;
+            // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NP / 2; ++q) {
+              const float2 r = make_float2(fmaxf(__uint_as_float(hv[2 * q]), 0.f),
+                                           fmaxf(__uint_as_float(hv[2 * q + 1]), 0.f));
+              const float4 w = w3[q];
+              acc0 = __ffma2_rn(r, make_float2(w.x, w.y), acc0);
+              acc1 = __ffma2_rn(r, make_float2(w.z, w.w), acc1);
+            }
+            const float o0 = acc0.x + acc0.y + b30, o1 = acc1.x + acc1.y + b31;
             const float upd = o0 * expf(o1 * kOutScale) * kOutScale;
             *p_ptr_prev = p_prev - lr * upd;
           }
-          tc_fence_before();
-          mbar_arrive(slot_empty + s);
         }
         p_ptr_prev = p_ptr_next;
         p_prev = p_next;
@@ -465,13 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   if (tid == 0 && *abort_flag) atomicOr(a.status, kStatusTimeout);
 }
 
-// Packs the layer-2 and layer-3 operands of every weight set (FP16,
-// canonical K-major) and its biases b2, b3 (FP32) from the caller-layout
-// weights at padded width hp.
+// Packs, per weight set, the layer-2 B operand (FP16, canonical K-major) and
+// the FP32 vectors the epilogue needs: b2[NP], the output weights as pairs
+// {W3[j][0], W3[j+1][0], W3[j][1], W3[j+1][1]} for even j, and b3[2]; padded
+// hidden units get zeros.
 template <int NP>
 __global__ void k_pack_tc(const float* weights, int hp, int set_size, int n_sets, uint8_t* out) {
   using G = Geom<NP>;
-  const int per = NP * NP + 16 * NP + NP + 4;
+  const int per = NP * NP + 3 * NP + 4;
   const int64_t total = (int64_t)n_sets * per;
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
        x += (int64_t)gridDim.x * blockDim.x) {
@@ -483,17 +496,20 @@ __global__ void k_pack_tc(const float* weights, int hp, int set_size, int n_sets
       const int n = r / NP, k = r % NP;
       const float v = (n < hp && k < hp) ? W[w_off_W2(hp) + k * hp + n] : 0.f;
       reinterpret_cast<__half*>(base)[f16_off(n, k, NP)] = __float2half_rn(v);
-    } else if ((r -= NP * NP) < 16 * NP) {    // B3[n][k] = W3[k][n], n < 2
-      const int n = r / NP, k = r % NP;
-      const float v = (n < 2 && k < hp) ? W[w_off_W3(hp) + 2 * k + n] : 0.f;
-      reinterpret_cast<__half*>(base + G::B2)[f16_off(n, k, NP)] = __float2half_rn(v);
-    } else {                                  // b2[NP], b3[2], pad
-      r -= 16 * NP;
-      float v = 0.f;
-      if (r < NP) v = r < hp ? W[w_off_b2(hp) + r] : 0.f;
-      else if (r < NP + 2) v = W[w_off_b3(hp) + (r - NP)];
-      reinterpret_cast<float*>(base + G::B2 + G::B3)[r] = v;
+      continue;
     }
+    r -= NP * NP;
+    float v = 0.f;
+    if (r < NP) {                             // b2
+      v = r < hp ? W[w_off_b2(hp) + r] : 0.f;
+    } else if (r < 3 * NP) {                  // W3 pairs
+      const int q = r - NP;                   // 4 floats per pair of hidden units
+      const int j = (q >> 2) * 2 + (q & 1), col = (q >> 1) & 1;
+      v = j < hp ? W[w_off_W3(hp) + 2 * j + col] : 0.f;
+    } else if (r < 3 * NP + 2) {              // b3
+      v = W[w_off_b3(hp) + (r - 3 * NP)];
+    }
+    reinterpret_cast<float*>(base + G::B2)[r] = v;
   }
 }
 

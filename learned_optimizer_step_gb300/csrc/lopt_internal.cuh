@@ -111,16 +111,21 @@ struct RowTerms {
   float sr[3];   // sqrt(r_k[i])
 };
 
-__device__ __forceinline__ RowTerms row_terms(const TensorDesc& d, const float inv_rho[3],
-                                              int64_t i) {
+// From the three row accumulators r_k[i] of an element's row.
+__device__ __forceinline__ RowTerms row_terms_of(const float r[3], const float inv_rho[3]) {
   RowTerms t;
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
-    float r = __ldg(d.r[k] + i);
-    t.rr[k] = fmul(r, inv_rho[k]);
-    t.sr[k] = fmul(r, frsqrt(fadd(r, kEps)));
+    t.rr[k] = fmul(r[k], inv_rho[k]);
+    t.sr[k] = fmul(r[k], frsqrt(fadd(r[k], kEps)));
   }
   return t;
+}
+
+__device__ __forceinline__ RowTerms row_terms(const TensorDesc& d, const float inv_rho[3],
+                                              int64_t i) {
+  const float r[3] = {__ldg(d.r[0] + i), __ldg(d.r[1] + i), __ldg(d.r[2] + i)};
+  return row_terms_of(r, inv_rho);
 }
 
 // Element-wise accumulator update (EMA of g and g^2), then the 28
