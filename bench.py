@@ -36,13 +36,16 @@ UNIT = "params/s"
 # Learned Optimizers in PyTorch", section "ステップ時間の削減": 99.59 ms,
 # hardware not stated): 86,415,592 params / 0.09959 s.
 PAGE_VIT_PARAMS_PER_S = 86415592 / 0.09959
+# rough single-thread speed of the fp64 oracle on a server core, used only to
+# size the reference arm's per-step sample
+ORACLE_PARAMS_PER_S = 1.2e6
 FP32_LANES_PER_SM = 128
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="vit_b16")
@@ -56,12 +59,16 @@ def parse():
 # CPU oracle timing (reported baseline; never the product path)
 # ---------------------------------------------------------------------------
 def _oracle_sample_shapes(wl, max_elems):
-    """Leading tensors of the workload, up to about max_elems parameters."""
+    """Leading tensors of the workload, up to about max_elems parameters.  A
+    leading matrix larger than the whole budget is cut to its first rows."""
     out, n = [], 0
     for name, shape in wl.shapes:
         k = 1
         for s in shape:
             k *= s
+        if not out and k > max_elems and len(shape) >= 2:
+            shape = (max(1, max_elems // shape[-1]),) + tuple(shape[1:])
+            name, k = name + "[leading rows]", shape[0] * shape[-1]
         if out and n + k > max_elems:
             continue
         out.append((name, shape))
@@ -139,6 +146,10 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            t0 = time.time()
+            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
+                time.sleep(0.02)
+            self.lines.clear()
         except Exception:
             self.proc = None
         return self
@@ -260,6 +271,23 @@ def algorithmic_bytes(states):
     return k0, k1, k2
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time: every rank's timed region ends with a barrier,
+    so the job's time is the maximum."""
+    if world <= 1:
+        return ms
+    import torch
+    x = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
+    return float(x.item())
+
+
+def job_throughput(numel_per_rank: int, world: int, steps: int, ms_total: float) -> float:
+    """Whole-job parameters per second: each replica updates its own list of
+    numel_per_rank parameters per step (weak scaling)."""
+    return numel_per_rank * world * steps / (ms_total / 1e3)
+
+
 def mlp_flops_per_element(hidden):
     return 2 * (39 * hidden + hidden * hidden + 2 * hidden)
 
@@ -314,15 +342,11 @@ def run_ours(args, rank, world, local_rank):
         stop.record(stream)
         barrier()
     eng.check()
-    ms_total = start.elapsed_time(stop)
+    ms_total = max_over_ranks(start.elapsed_time(stop), world, dev)
     kms, klaunch = eng.kernel_times()
     eng.set_kernel_timing(False)
-    if world > 1:
-        x = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(x.item())
     ms_step = ms_total / args.steps
-    value = numel * world * args.steps / (ms_total / 1e3)
+    value = job_throughput(numel, world, args.steps, ms_total)
 
     # ---- end to end through the public API with host buffers ----
     h_g = torch.empty(nflat, dtype=torch.float32, pin_memory=True)
@@ -339,12 +363,8 @@ def run_ours(args, rank, world, local_rank):
         t += 1
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        x = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(x, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(x.item())
-    e2e_value = numel * world * e2e_steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_throughput(numel, world, e2e_steps, e2e_ms)
 
     if rank != 0:
         return None
@@ -410,7 +430,9 @@ def run_reference(args, rank):
         return None
     import synth
     wl = synth.workloads()[args.workload]
-    res = run_oracle_subprocess(args.workload, 1_000_000, args.warmup + args.steps)
+    # a bounded sample per step: the whole run stays near two minutes
+    per_step = int(min(1_000_000, max(65_536, 120 * ORACLE_PARAMS_PER_S / (args.warmup + args.steps))))
+    res = run_oracle_subprocess(args.workload, per_step, args.warmup + args.steps)
     times = res["step_s"][args.warmup:]
     tot = sum(times)
     value = res["elements"] * len(times) / tot
