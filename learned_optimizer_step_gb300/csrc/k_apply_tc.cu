@@ -10,28 +10,33 @@
 //
 // One persistent CTA per SM, warp-specialised, linked by mbarriers:
 //   warp 16      producer: bulk-copies (cp.async.bulk, one array per lane) p,
-//                g, m0..2, v of the next 8 tiles of a work unit into a ring
-//                of shared-memory stages;
+//                g, m0..2, v of up to 8 tiles of a work unit into a ring of
+//                shared-memory stages, and writes p, m0..2, v of a stage back
+//                with bulk copies once every thread has left it;
 //   warps 8-15   two feature warpgroups (alternate tiles): EMA update,
 //                features, normalisation, FP16 A operand of layer 1 into the
-//                tile slot's tensor memory; they also store the updated
-//                accumulators m and v;
+//                tile slot's tensor memory; the updated m and v go back into
+//                the stage;
 //   warp 17      MMA issuer (one thread);
 //   warps 0-7    two epilogue warpgroups (alternate tiles): ReLU + FP16 A
 //                operand of layer 2 (in tensor memory) and the b2 preset of
-//                its accumulator; then ReLU(h2), the two-unit output layer in
-//                FP32 on the CUDA cores, and the update of p.
+//                its accumulator; then ReLU(h2), the two-unit output layer
+//                in FP32 on the CUDA cores, and the update of p in the stage.
 // A tile is 128 consecutive elements of one tensor (one per TMEM lane).  A
 // tile slot is a set of tensor-memory columns: the FP32 accumulator (NP
 // columns) and the FP16 A operand of the next MMA (16 columns); the A
-// operands never pass through shared memory.
+// operands never pass through shared memory.  Per-tensor data (scales,
+// 1/rho, row/column accumulator addresses) travel with each stage in a
+// small record, so the feature warps keep no per-tensor state.
 //
 // Small MMAs (M=128, N<=32) cost about 40-50 cycles of the SM's MMA pipe
 // each, whatever their K, and an MMA's result reaches a waiting thread about
 // a thousand cycles after issue.  So a tile uses few MMAs (FP16 operands,
-// K = 32 for layer 1 and K = NP for layer 2: 4 MMAs at NP = 32, biases
-// without extra K columns, one tcgen05.commit per issue iteration) and only
-// two MMA round trips: the output layer (two units) runs on the CUDA cores.
+// K = 32 for layer 1 with b1 against a constant 1 in the A operand, and
+// K = NP + 16 for layer 2 whose last K-step multiplies a constant tensor-
+// memory block (1, 0, ...) with the b2 row of B: 5 MMAs at NP = 32, one
+// tcgen05.commit per issue iteration) and only two MMA round trips: the
+// output layer (two units) runs on the CUDA cores.
 // Stages of different tiles overlap with fixed lags chosen for the largest
 // slack around that latency: in iteration k the MMA thread issues layer 1 of
 // tile k and layer 2 of tile k-5 (K-steps interleaved), then commits once;
@@ -56,25 +61,59 @@ namespace {
 
 constexpr int kTile = 128;                // elements per tile (= TMEM lanes)
 constexpr int kThreads = 18 * 32;         // 8 epilogue + 8 feature + producer + MMA warps
-constexpr int kStageTiles = 8;            // tiles per input stage (4 KB per array)
+constexpr int kStageTiles = 8;            // tiles per stage (4 KB per array)
 constexpr int kStageElems = kStageTiles * kTile;
-constexpr int kRingStages = 5;            // input stages
-constexpr int kStageBytes = 6 * kStageElems * 4;
+constexpr int kArrays = 6;                // p, g, m0, m1, m2, v
+constexpr int kRingStages = 6;            // stages held in shared memory
+constexpr int kStageBytes = kArrays * kStageElems * 4;
+constexpr int kStageUsers = 4 * kTile;    // feature and epilogue threads, one arrival each per stage
 constexpr int kDone = 8;                  // commit barriers (one per MMA iteration)
 constexpr int kLag2 = 5;                  // MMA iteration k: layer 2 of tile k-5
 constexpr int kE1 = 4, kE2 = 8;           // epilogue step m: tiles m-4, m-8
 constexpr int kProducerWarp = 16, kMmaWarp = 17;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
+// Where stage array q (p, g, m0, m1, m2, v) of a tensor lives.
+__device__ __forceinline__ float* stage_array(const TensorDesc& d, int q) {
+  return q == 0 ? d.p : q == 1 ? const_cast<float*>(d.g) : q == 5 ? d.v : d.m[q - 2];
+}
+
+// A tensor's tiles move through shared memory by bulk copies when every
+// array is 16-byte aligned and every stage is a whole number of 16-byte
+// words; otherwise the feature and epilogue warps read and write its
+// arrays in global memory themselves.
+__device__ __forceinline__ bool staged(const TensorDesc& d) { return d.vec4 && (d.N & 3) == 0; }
+
+// What the tiles of one ring slot need to know about their tensor, written
+// by the producer when it loads the slot (and read again when it writes the
+// slot back): the feature warps then keep no per-tensor state.
+struct StageRec {
+  float        sc[kStats];   // normalisation scales
+  float        inv_rho[3];
+  int32_t      tensor;
+  const float* c[3];         // column accumulators
+  const float* r[3];         // row accumulators
+  int64_t      e0;           // first element of the stage
+  int64_t      i0;           // its row and column
+  int32_t      j0;
+  int32_t      C;
+  uint32_t     bytes;        // bytes per array; 0: not staged (nothing to write back)
+  float        invC;         // 1 / C
+};
+static_assert(sizeof(StageRec) % 16 == 0, "stage records stay 16-byte aligned");
+
 template <int NP>
 struct Geom {
   static constexpr int ACols = 16;                     // A operand: 32 FP16 per row
   static constexpr int SlotCols = NP + ACols;          // accumulator + A operand
-  static constexpr int S = 512 / SlotCols < 16 ? 512 / SlotCols : 16;   // tiles in flight
+  static constexpr int OneCols = 8;                    // constant A block (1, 0, ..., 0) for b2
+  static constexpr int S = (512 - OneCols) / SlotCols < 16 ? (512 - OneCols) / SlotCols : 16;   // tiles in flight
+  static constexpr int OneCol = S * SlotCols;          // its first column
+  static constexpr int K2 = NP + 16;                   // layer 2: h1 (NP) then the bias block (16)
   static constexpr int SBO1 = 32 * 16;                 // layer-1 B operand: K = 32
-  static constexpr int SBO = NP * 16;                  // layer-2/3 B operands: K = NP
+  static constexpr int SBO = K2 * 16;                  // layer-2 B operand: K = K2
   static constexpr int B1 = NP * 32 * 2;
-  static constexpr int B2 = NP * NP * 2;
+  static constexpr int B2 = NP * K2 * 2;
   static constexpr int Aux = (3 * NP + 4) * 4;         // b2[NP], W3 pairs[NP][2], b3[2], pad
   static constexpr int Set = (B2 + Aux + 1023) / 1024 * 1024;   // packed per-set stride
   static constexpr int oRing = 0;
@@ -82,44 +121,61 @@ struct Geom {
   static constexpr int oB2 = oB1 + B1;                  // B2, b2, W3, b3 as packed
   static constexpr int oBar = (oB2 + Set + 15) / 16 * 16;
   static constexpr int nBars = 2 * kRingStages + 3 * S + kDone;
-  static constexpr int oInfo = oBar + nBars * 8;
+  static constexpr int oRec = (oBar + nBars * 8 + 15) / 16 * 16;   // records are read as float4
+  static constexpr int oInfo = oRec + kRingStages * (int)sizeof(StageRec);
   static constexpr int Smem = oInfo + 64;
   static constexpr int TmemCols = 512;
   static constexpr uint32_t ID12 = instr_desc(0, 128, NP);
   static_assert(Smem <= 232448, "shared memory of one CTA");
-  static_assert(S * SlotCols <= 512 && S > kE2, "tensor memory columns / pipeline depth");
+  static_assert(OneCol + OneCols <= 512 && S > kE2, "tensor memory columns / pipeline depth");
+  static_assert(oRec % 16 == 0 && sizeof(StageRec) % 16 == 0, "16-byte aligned stage records");
 };
 
-// Walks tiles in order: units [u, u1), 128-element tiles each.
-struct TileWalk {
+// Walks the tiles of a session in order (work units [u, u1), 128-element
+// tiles each) and tracks the ring slot and round parity of each tile's stage.
+// A stage holds up to kStageTiles consecutive tiles of one work unit.
+struct Walk {
   const Unit* units;
   const TensorDesc* desc;
-  int64_t u, u1;
-  int tensor;
-  int64_t ustart, start, end;   // unit start, tile start, unit end
-  __device__ void init(const Unit* un, const TensorDesc* de, int64_t b, int64_t e) {
-    units = un; desc = de; u = b; u1 = e;
+  int32_t u, u1;
+  int32_t tensor;
+  int32_t off, len;   // tile offset in its unit, unit length (elements)
+  int64_t base;       // first element of the unit
+  int32_t st;         // ring slot of the tile's stage
+  uint32_t ph;        // parity of the slot's round
+  __device__ void init(const Unit* un, const TensorDesc* de, int32_t b, int32_t e) {
+    units = un; desc = de; u = b; u1 = e; st = 0; ph = 0;
     load();
   }
   __device__ void load() {
     if (u < u1) {
       const Unit x = units[u];
       tensor = x.tensor;
-      ustart = start = (int64_t)x.local * kApplyChunk;
-      end = min(desc[tensor].N, start + (int64_t)kApplyChunk);
+      base = (int64_t)x.local * kApplyChunk;
+      len = (int32_t)min(desc[tensor].N - base, (int64_t)kApplyChunk);
+      off = 0;
     }
   }
-  __device__ void next() {
-    start += kTile;
-    if (start >= end) { ++u; load(); }
+  // Moves to the next tile; true when it opens a new stage (st and ph then
+  // describe the new stage).
+  __device__ bool next() {
+    off += kTile;
+    if (off >= len) {
+      if (++u >= u1) return false;
+      load();
+    } else if (off & (kStageElems - 1)) {
+      return false;
+    }
+    if (++st == kRingStages) { st = 0; ph ^= 1u; }
+    return true;
   }
 };
 
-__device__ __forceinline__ int64_t unit_tiles(const StepArgs& a, int64_t u) {
+__device__ __forceinline__ int32_t unit_tiles(const StepArgs& a, int32_t u) {
   const Unit x = a.units[u];
   const int64_t st = (int64_t)x.local * kApplyChunk;
   const int64_t en = min(a.desc[x.tensor].N, st + (int64_t)kApplyChunk);
-  return (en - st + kTile - 1) / kTile;
+  return (int32_t)((en - st + kTile - 1) / kTile);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight work).
@@ -127,9 +183,21 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint6
   if (mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < (1u << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((it & 15) == 0 && global_ns() - t0 > limit_ns) return;
+    if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return;
+    if (global_ns() - t0 > limit_ns) return;
   }
+}
+
+// A feature or epilogue thread is done with the stage in slot st (round
+// parity ph).  It first waits until that stage has been loaded, so that the
+// slot has left its previous round, then makes its shared-memory writes
+// visible to the bulk copies and arrives.
+__device__ __forceinline__ bool leave_stage(uint64_t* ring_full, uint64_t* stage_done, int st, uint32_t ph,
+                                            volatile int* abort_flag) {
+  if (!mbar_wait_or_abort(ring_full + st, ph, kWaitNs, abort_flag)) return false;
+  fence_proxy_async();
+  mbar_arrive(stage_done + st);
+  return true;
 }
 
 // ReLU + FP16 of one accumulator row, packed two per 32-bit column (16
@@ -160,12 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   float* ring = reinterpret_cast<float*>(smem + G::oRing);
   uint64_t* ring_full = reinterpret_cast<uint64_t*>(smem + G::oBar);
-  uint64_t* ring_empty = ring_full + R;
-  uint64_t* a1_full = ring_empty + R;
+  uint64_t* stage_done = ring_full + R;
+  uint64_t* a1_full = stage_done + R;
   uint64_t* a2_full = a1_full + S;
   uint64_t* slot_empty = a2_full + S;
   uint64_t* done = slot_empty + S;
-  int64_t* info = reinterpret_cast<int64_t*>(smem + G::oInfo);   // session: end unit, tiles
+  StageRec* rec = reinterpret_cast<StageRec*>(smem + G::oRec);
+  int32_t* info = reinterpret_cast<int32_t*>(smem + G::oInfo);   // session: end unit, tiles
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::oInfo + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + G::oInfo + 40);
 
@@ -178,22 +247,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (warp < 4) {   // the constant A block of layer 2's bias K-step: 1.0h, then zeros
+    uint32_t one[8] = {0x00003C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st8(tmem + ((uint32_t)(warp * 32) << 16) + G::OneCol, one);
+    tmem_wait_st();
+  }
+  tc_fence_before();
 
-  const int64_t U = a.n_units;
-  const int64_t u_first = (int64_t)blockIdx.x * U / gridDim.x;
-  const int64_t u_last = (int64_t)(blockIdx.x + 1) * U / gridDim.x;
+  const int32_t U = a.n_units;
+  const int32_t u_first = (int32_t)((int64_t)blockIdx.x * U / gridDim.x);
+  const int32_t u_last = (int32_t)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
 
-  for (int64_t u0 = u_first; u0 < u_last;) {
+  for (int32_t u0 = u_first; u0 < u_last;) {
     // ---- session set-up: tiles sharing one weight set --------------------------
     if (tid == 0) {
       const int wset = a.desc[a.units[u0].tensor].wset;
-      int64_t u1 = u0, K = 0;
+      int32_t u1 = u0, K = 0;
       while (u1 < u_last && a.desc[a.units[u1].tensor].wset == wset) K += unit_tiles(a, u1++);
       info[0] = u1;
       info[1] = K;
       for (int r = 0; r < R; ++r) {
         mbar_init(ring_full + r, 1);
-        mbar_init(ring_empty + r, 2 * kTile);   // every feature thread, once per stage
+        mbar_init(stage_done + r, kStageUsers);
       }
       for (int s = 0; s < S; ++s) {
         mbar_init(a1_full + s, kTile);
@@ -214,150 +289,200 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
     }
     fence_proxy_async();
     __syncthreads();
-    const int64_t u1 = info[0], K = info[1];
+    const int32_t u1 = info[0], K = info[1];
     if (*abort_flag) break;
 
     if (warp == kProducerWarp) {
       // ------------------------------ producer -------------------------------
-      // A stage holds up to 8 consecutive tiles of one work unit; lane q < 6
-      // copies array q of the stage.
-      int64_t n_st = 0;
-      for (int64_t u = u0; u < u1 && !*abort_flag; ++u) {
+      // Lane q < 6 moves array q of every stage.  Before a slot is loaded
+      // again, the stage it held is written back (p, m0..2, v) once every
+      // feature and epilogue thread has left it.
+      auto write_back = [&](int st) {
+        const StageRec r = rec[st];
+        if (r.bytes != 0 && lane < kArrays && lane != 1) {
+          bulk_s2g(stage_array(a.desc[r.tensor], lane) + r.e0, ring + st * (kArrays * kStageElems) + lane * kStageElems,
+                   r.bytes);
+          bulk_commit();
+          bulk_wait_read_all();   // the slot may be refilled once its contents have been read
+        }
+        __syncwarp();
+      };
+      int32_t n = 0;      // stages issued
+      int st = 0;         // slot of stage n
+      uint32_t ph = 0;    // its round parity
+      bool stop = false;
+      for (int32_t u = u0; u < u1 && !stop; ++u) {
         const Unit x = a.units[u];
         const TensorDesc& d = a.desc[x.tensor];
-        const bool vec = d.vec4 && (d.C % 4 == 0);
-        const int64_t ue = min(d.N, (int64_t)x.local * kApplyChunk + kApplyChunk);
-        const float* src = lane == 0 ? d.p : lane == 1 ? d.g : lane == 2 ? d.m[0] : lane == 3 ? d.m[1]
-                         : lane == 4 ? d.m[2] : d.v;
-        bool stop = false;
-        for (int64_t e0 = (int64_t)x.local * kApplyChunk; e0 < ue; e0 += kStageElems, ++n_st) {
-          const int st = (int)(n_st % R);
-          if (!mbar_wait_or_abort(ring_empty + st, (uint32_t)((n_st / R) & 1) ^ 1u, kWaitNs, abort_flag)) {
-            stop = true;
-            break;
+        const bool stg = staged(d);
+        const int64_t ub = (int64_t)x.local * kApplyChunk;
+        const int64_t ue = min(d.N, ub + kApplyChunk);
+        const float* src = stage_array(d, lane < kArrays ? lane : 0);
+        for (int64_t e0 = ub; e0 < ue; e0 += kStageElems) {
+          if (n >= R) {   // the slot's previous stage: round ph ^ 1
+            if (!mbar_wait_or_abort(stage_done + st, ph ^ 1u, kWaitNs, abort_flag)) {
+              stop = true;
+              break;
+            }
+            write_back(st);
           }
           const uint32_t bytes = (uint32_t)(min((int64_t)kStageElems, ue - e0) * 4);
+          StageRec& rc = rec[st];
+          if (lane < kStats) rc.sc[lane] = a.aux[x.tensor].scale[lane];
+          else if (lane < kStats + 3) rc.inv_rho[lane - kStats] = a.aux[x.tensor].inv_rho[lane - kStats];
+          else if (lane == 31) {
+            rc.tensor = x.tensor;
+            rc.e0 = e0;
+            rc.i0 = e0 / d.C;
+            rc.j0 = (int32_t)(e0 - rc.i0 * d.C);
+            rc.C = (int32_t)d.C;
+            rc.invC = 1.0f / (float)d.C;
+            rc.bytes = stg ? bytes : 0u;
+          }
+          if (lane < 3) rc.c[lane] = d.c[lane];
+          else if (lane < 6) rc.r[lane - 3] = d.r[lane - 3];
+          __syncwarp();
           if (lane == 0) {
-            if (vec) mbar_arrive_expect_tx(ring_full + st, 6 * bytes);
-            else mbar_arrive(ring_full + st);   // feature warps read global memory directly
+            if (stg) mbar_arrive_expect_tx(ring_full + st, kArrays * bytes);
+            else mbar_arrive(ring_full + st);
           }
           __syncwarp();
-          if (vec && lane < 6) bulk_g2s(ring + st * (6 * kStageElems) + lane * kStageElems, src + e0, bytes,
-                                        ring_full + st);
+          if (stg && lane < kArrays)
+            bulk_g2s(ring + st * (kArrays * kStageElems) + lane * kStageElems, src + e0, bytes, ring_full + st);
+          ++n;
+          if (++st == R) { st = 0; ph ^= 1u; }
         }
-        if (stop) break;
       }
-      if (*abort_flag) {   // let copies already issued land before teardown
-        for (int64_t kk = (n_st > R ? n_st - R : 0); kk < n_st; ++kk)
-          mbar_drain(ring_full + kk % R, (uint32_t)((kk / R) & 1), kWaitNs / 10);
+      // the stages still in the ring, oldest first
+      for (int32_t x = (n > R ? n - R : 0); x < n && !stop; ++x) {
+        const int xs = x % R;
+        if (!mbar_wait_or_abort(stage_done + xs, (uint32_t)((x / R) & 1), kWaitNs, abort_flag)) {
+          stop = true;
+          break;
+        }
+        write_back(xs);
       }
+      if (stop) {   // let loads already issued land before teardown
+        for (int32_t x = (n > R ? n - R : 0); x < n; ++x)
+          mbar_drain(ring_full + x % R, (uint32_t)((x / R) & 1), kWaitNs / 10);
+      }
+      bulk_wait_all();   // every write-back complete before the session ends
     } else if (warp >= 8 && warp < 16) {
       // --------------------------- feature warpgroups ------------------------
+      // Group grp takes the tiles k with k % 2 == grp.  Every thread walks
+      // all tiles so that it leaves each stage exactly once.
       const int grp = (warp - 8) >> 2;
       const int t = tid - 256 - 128 * grp;
       const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      TileWalk w;
+      Walk w;
       w.init(a.units, a.desc, u0, u1);
-      int cur = -1;
-      bool vec = false, have_ij = false;
-      int64_t i = 0, j = 0, last_e = 0, di = 0, dj = 0;
-      float inv_rho[3] = {0.f, 0.f, 0.f};
-      float sc[kStats];
-#pragma unroll
-      for (int q = 0; q < kStats; ++q) sc[q] = 0.f;
-      // input stage of the current tile: counter, ring index, offset in it
-      int64_t n_st = -1;
-      int st = 0, st_off = 0;
-      int64_t k = 0;
-      for (; k < K; ++k, w.next()) {
-        const int64_t in_unit = w.start - w.ustart;
-        if (in_unit % kStageElems == 0) {   // this tile opens a new stage
-          if (n_st >= 0) mbar_arrive(ring_empty + st);   // done with the previous one
-          ++n_st;
-          st = (int)(n_st % R);
+      int s = grp;          // slot of this group's next tile
+      uint32_t sph = 0;     // its round parity
+      bool ok = true;
+      for (int32_t k = 0; k < K; ++k) {
+        if (k > 0) {
+          const int pst = w.st;
+          const uint32_t pph = w.ph;
+          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) {
+            ok = false;
+            break;
+          }
         }
-        st_off = (int)(in_unit % kStageElems);
-        if ((int)(k & 1) != grp) continue;
-        const int s = (int)(k % S);
-        if (!mbar_wait_or_abort(slot_empty + s, (uint32_t)((k / S) & 1) ^ 1u, kWaitNs, abort_flag)) break;
-        if (!mbar_wait_or_abort(ring_full + st, (uint32_t)((n_st / R) & 1), kWaitNs, abort_flag)) break;
-        const TensorDesc& d = a.desc[w.tensor];
-        if (w.tensor != cur) {
-          cur = w.tensor;
-          vec = d.vec4 && (d.C % 4 == 0);
-#pragma unroll
-          for (int q = 0; q < 3; ++q) inv_rho[q] = a.aux[cur].inv_rho[q];
-#pragma unroll
-          for (int q = 0; q < kStats; ++q) sc[q] = a.aux[cur].scale[q];
-          di = (2 * kTile) / d.C;
-          dj = (2 * kTile) - di * d.C;
-          have_ij = false;
+        if ((k & 1) != grp) continue;
+        if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag) ||
+            !mbar_wait_or_abort(ring_full + w.st, w.ph, kWaitNs, abort_flag)) {
+          ok = false;
+          break;
         }
-        const int64_t e = w.start + t;
-        const bool valid = e < w.end;
+        const StageRec& rc = rec[w.st];
+        const bool stg = rc.bytes != 0;
+        const int x = (w.off & (kStageElems - 1)) + t;   // element offset in the stage
+        const bool valid = w.off + t < w.len;
+        const int64_t e = rc.e0 + x;
+        float* rs = ring + w.st * (kArrays * kStageElems) + x;
         float p = 0.f, g = 0.f, m[3] = {0.f, 0.f, 0.f}, v = 0.f;
-        if (vec) {
-          const float* rs = ring + st * (6 * kStageElems) + st_off + t;
-          if (valid) {
+        float c[3] = {0.f, 0.f, 0.f};
+        float r[3] = {0.f, 0.f, 0.f};
+        if (valid) {
+          if (stg) {
             p = rs[0]; g = rs[kStageElems]; m[0] = rs[2 * kStageElems]; m[1] = rs[3 * kStageElems];
             m[2] = rs[4 * kStageElems]; v = rs[5 * kStageElems];
-          }
-        } else if (valid) {
-          p = __ldg(d.p + e); g = __ldg(d.g + e); v = __ldg(d.v + e);
-#pragma unroll
-          for (int q = 0; q < 3; ++q) m[q] = __ldg(d.m[q] + e);
-        }
-        float c[3] = {0.f, 0.f, 0.f};
-        RowTerms rt;
-#pragma unroll
-        for (int q = 0; q < 3; ++q) { rt.rr[q] = 0.f; rt.sr[q] = 0.f; }
-        if (valid) {
-          if (have_ij && e == last_e + 2 * kTile) {
-            i += di; j += dj;
-            if (j >= d.C) { j -= d.C; ++i; }
           } else {
-            i = e / d.C; j = e - i * d.C;
-          }
-          last_e = e;
-          have_ij = true;
+            const TensorDesc& d = a.desc[rc.tensor];
+            p = d.p[e]; g = __ldg(d.g + e); v = d.v[e];
 #pragma unroll
-          for (int q = 0; q < 3; ++q) c[q] = __ldg(d.c[q] + j);
-          rt = row_terms(d, inv_rho, i);
-        } else {
-          have_ij = false;
+            for (int q = 0; q < 3; ++q) m[q] = d.m[q][e];
+          }
+          // row and column of the element
+          // j0 + x < C + kStageElems, so a float quotient is exact to within one
+          const uint32_t C = (uint32_t)rc.C;
+          int64_t i = rc.i0;
+          uint32_t j = (uint32_t)rc.j0 + (uint32_t)x;
+          if (j >= C) {
+            uint32_t q = (uint32_t)((float)j * rc.invC);
+            int32_t rem = (int32_t)(j - q * C);
+            if (rem < 0) { --q; rem += (int32_t)C; }
+            else if (rem >= (int32_t)C) { ++q; rem -= (int32_t)C; }
+            i += q;
+            j = (uint32_t)rem;
+          }
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            c[q] = __ldg(rc.c[q] + j);
+            r[q] = __ldg(rc.r[q] + i);
+          }
         }
+        float inv_rho[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) inv_rho[q] = rc.inv_rho[q];
+        const RowTerms rt = row_terms_of(r, inv_rho);
         float f[kStats];
         lopt_features(p, g, m, v, rt, c, f);
         if (valid) {
+          if (stg) {
+            rs[2 * kStageElems] = m[0]; rs[3 * kStageElems] = m[1]; rs[4 * kStageElems] = m[2];
+            rs[5 * kStageElems] = v;
+          } else {
+            const TensorDesc& d = a.desc[rc.tensor];
 #pragma unroll
-          for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
-          d.v[e] = v;
+            for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
+            d.v[e] = v;
+          }
         }
         // normalised features, FP16, into this lane's row of the slot's A
         // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
         uint32_t av[16];
+        const float4* sc4 = reinterpret_cast<const float4*>(rc.sc);
 #pragma unroll
-        for (int q = 0; q < 14; ++q) av[q] = f16x2(f[2 * q] * sc[2 * q], f[2 * q + 1] * sc[2 * q + 1]);
+        for (int q = 0; q < 7; ++q) {
+          const float4 sq = sc4[q];
+          const float2 lo = __fmul2_rn(make_float2(f[4 * q], f[4 * q + 1]), make_float2(sq.x, sq.y));
+          const float2 hi = __fmul2_rn(make_float2(f[4 * q + 2], f[4 * q + 3]), make_float2(sq.z, sq.w));
+          av[2 * q] = f16x2(lo.x, lo.y);
+          av[2 * q + 1] = f16x2(hi.x, hi.y);
+        }
         av[14] = 0x00003C00u;   // 1.0h, 0
         av[15] = 0u;
         tmem_st16(t_lane + s * G::SlotCols + NP, av);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(a1_full + s);
+        s += 2;
+        if (s >= S) { s -= S; sph ^= 1u; }
       }
-      if (k == K && n_st >= 0) mbar_arrive(ring_empty + st);
+      if (ok && K > 0) leave_stage(ring_full, stage_done, w.st, w.ph, abort_flag);
     } else if (warp == kMmaWarp) {
       // ------------------------------- MMA issuer ----------------------------
       if (lane == 0) {
         const uint64_t dB1 = smem_desc(s_base + G::oB1, 128, G::SBO1);
         const uint64_t dB2 = smem_desc(s_base + G::oB2, 128, G::SBO);
-        const int k_end = (int)K + kLag2;
+        const int k_end = K + kLag2;
         // slot index and phase of tile k and of tile k - kLag2, kept incrementally
         int s1 = 0, s2 = S - kLag2;
         uint32_t p1 = 0, p2 = 1;
         int k = 0;
         for (; k < k_end; ++k) {
-          const bool do1 = k < (int)K;
+          const bool do1 = k < K;
           const bool do2 = k >= kLag2;
           if (do1 && !mbar_wait_or_abort(a1_full + s1, p1, kWaitNs, abort_flag)) break;
           if (do2 && !mbar_wait_or_abort(a2_full + s2, p2, kWaitNs, abort_flag)) break;
@@ -379,85 +504,134 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       }
     } else if (warp < 8) {
       // ------------------------------ epilogue -------------------------------
-      // Group h takes the tiles k with k % 2 == h.  In step m it finishes
-      // layer 1 of tile m-4 (ReLU, FP16 A operand of layer 2, b2 preset of
-      // its accumulator) and the rest of tile m-8 (ReLU(h2), output layer,
-      // update); it loads p of tile m-6 for the update two steps later.
+      // Group h takes the steps m with m % 2 == h.  Step m finishes layer 1
+      // of tile t1 = m-4 (ReLU, FP16 A operand of layer 2), then the rest of
+      // tile t2 = m-8 (ReLU(h2), output layer, update of p).
       const int h = warp >> 2;
       const int t = tid - 128 * h;
       const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
       const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
       const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
       const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
-      TileWalk wp;   // tile m-6 of this group
-      wp.init(a.units, a.desc, u0, u1);
-      if (h == 1) wp.next();
       const float lr = a.lr;
-      float* p_ptr_prev = nullptr;
-      float p_prev = 0.f;
-      for (int64_t m = h; m - kE2 < K; m += 2) {
-        if (*abort_flag) break;
-        const int64_t t1 = m - kE1, t2 = m - kE2, tp = m - (kE2 - 2);
-        float* p_ptr_next = nullptr;
-        float p_next = 0.f;
-        if (tp >= 0 && tp < K) {
-          const int64_t e = wp.start + t;
-          if (e < wp.end) {
-            p_ptr_next = a.desc[wp.tensor].p + e;
-            p_next = *p_ptr_next;
-          }
-          wp.next();
-          wp.next();
+      Walk w;   // at tile wk; the stages behind it have been left
+      w.init(a.units, a.desc, u0, u1);
+      int32_t wk = 0;
+      bool ok = true;
+      for (int32_t m = h; m - kE2 < K; m += 2) {
+        if (*abort_flag) { ok = false; break; }
+        const int32_t t1 = m - kE1, t2 = m - kE2;
+        const bool e1 = t1 >= 0 && t1 < K, e2 = t2 >= 0;
+        const int s1 = e1 ? t1 % S : 0, s2 = e2 ? t2 % S : 0;
+        while (e2 && wk < t2) {
+          ++wk;
+          const int pst = w.st;
+          const uint32_t pph = w.ph;
+          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) { ok = false; break; }
         }
-        if (t1 >= 0 && t1 < K) {
-          const int s = (int)(t1 % S);
-          if (!mbar_wait_or_abort(done + (t1 % kDone), (uint32_t)((t1 / kDone) & 1), kWaitNs, abort_flag)) break;
+        if (!ok) break;
+        if (e1) {   // layer 1 of tile t1: FP16 A operand of layer 2
+          if (!mbar_wait_or_abort(done + (t1 & (kDone - 1)), (uint32_t)((t1 / kDone) & 1), kWaitNs, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t col = t_lane + s * G::SlotCols;
-          uint32_t hv[NP], av[16], b2[NP];
-          tmem_ld_row<NP>(col, hv);
+          const uint32_t col = t_lane + s1 * G::SlotCols;
+          uint32_t av[16];
+          {
+            uint32_t h1[NP];
+            tmem_ld_row<NP>(col, h1);
+            tmem_wait_ld();
+            pack_relu_row<NP>(h1, av);
+          }
+          tmem_st16(col + NP, av);
+          uint32_t b2[NP];
 #pragma unroll
           for (int q = 0; q < NP; q += 4) {
             const float4 b = *reinterpret_cast<const float4*>(aux + q);
             b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
             b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
           }
-          tmem_wait_ld();
-          pack_relu_row<NP>(hv, av);
-          tmem_st16(col + NP, av);
           tmem_st_row<NP>(col, b2);
+        }
+        if (e1) {
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(a2_full + s);
+          mbar_arrive(a2_full + s1);
         }
-        if (t2 >= 0 && t2 < K) {
-          const int s = (int)(t2 % S);
-          const int64_t it = t2 + kLag2;
-          if (!mbar_wait_or_abort(done + (it % kDone), (uint32_t)((it / kDone) & 1), kWaitNs, abort_flag)) break;
+        if (e2) {   // rest of tile t2: its slot is freed as soon as h2 is read
+          const int32_t it = t2 + kLag2;
+          if (!mbar_wait_or_abort(done + (it & (kDone - 1)), (uint32_t)((it / kDone) & 1), kWaitNs, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          uint32_t hv[NP];
-          tmem_ld_row<NP>(t_lane + s * G::SlotCols, hv);
+          uint32_t h2[NP];
+          tmem_ld_row<NP>(t_lane + s2 * G::SlotCols, h2);
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(slot_empty + s);   // the slot's tensor memory is no longer read
-          if (p_ptr_prev) {
-            // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          mbar_arrive(slot_empty + s2);
+          if (w.off + t < w.len) {
+            // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3, in
+            // chunks of 8 hidden units whose weights are loaded one chunk
+            // ahead (shared-memory latency off the FMA chains)
+            constexpr int kCh = NP / 8;
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};   // (o0, o1) x 2 chains
+            float4 wcur[4], wnext[4];
 #pragma unroll
-            for (int q = 0; q < NP / 2; ++q) {
-              const float2 r = make_float2(fmaxf(__uint_as_float(hv[2 * q]), 0.f),
-                                           fmaxf(__uint_as_float(hv[2 * q + 1]), 0.f));
-              const float4 w = w3[q];
-              acc0 = __ffma2_rn(r, make_float2(w.x, w.y), acc0);
-              acc1 = __ffma2_rn(r, make_float2(w.z, w.w), acc1);
+            for (int q = 0; q < 4; ++q) wcur[q] = w3[q];
+#pragma unroll
+            for (int ch = 0; ch < kCh; ++ch) {
+              if (ch + 1 < kCh) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wnext[q] = w3[4 * (ch + 1) + q];
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int u = 8 * ch + 2 * q;
+                const float2 hr = make_float2(fmaxf(__uint_as_float(h2[u]), 0.f),
+                                              fmaxf(__uint_as_float(h2[u + 1]), 0.f));
+                acc[(q & 1) * 2] = __ffma2_rn(hr, make_float2(wcur[q].x, wcur[q].y), acc[(q & 1) * 2]);
+                acc[(q & 1) * 2 + 1] = __ffma2_rn(hr, make_float2(wcur[q].z, wcur[q].w), acc[(q & 1) * 2 + 1]);
+              }
+              if (ch + 1 < kCh) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wcur[q] = wnext[q];
+              }
             }
-            const float o0 = acc0.x + acc0.y + b30, o1 = acc1.x + acc1.y + b31;
-            const float upd = o0 * expf(o1 * kOutScale) * kOutScale;
-            *p_ptr_prev = p_prev - lr * upd;
+            const float o0 = (acc[0].x + acc[0].y) + (acc[2].x + acc[2].y) + b30;
+            const float o1 = (acc[1].x + acc[1].y) + (acc[3].x + acc[3].y) + b31;
+            // exp(x) = 2^(x log2 e) with the PTX ex2.approx instruction
+            // (relative error below 2^-22); here |x| = |o1| * 1e-3 is small
+            float ex;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
+            const float upd = o0 * ex * kOutScale;
+            const StageRec& rc = rec[w.st];
+            if (rc.bytes != 0) {
+              float* pp = ring + w.st * (kArrays * kStageElems) + (w.off & (kStageElems - 1)) + t;
+              *pp = *pp - lr * upd;
+            } else {
+              float* pp = a.desc[rc.tensor].p + (w.base + w.off + t);
+              *pp = *pp - lr * upd;
+            }
           }
         }
-        p_ptr_prev = p_ptr_next;
-        p_prev = p_next;
+        if (e2 && wk + 1 < K) {   // leave t2's stage as soon as the next tile opens another one
+          ++wk;
+          const int pst = w.st;
+          const uint32_t pph = w.ph;
+          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) { ok = false; break; }
+        }
+      }
+      if (ok && K > 0) {
+        while (ok && wk < K - 1) {
+          ++wk;
+          const int pst = w.st;
+          const uint32_t pph = w.ph;
+          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) ok = false;
+        }
+        if (ok) leave_stage(ring_full, stage_done, w.st, w.ph, abort_flag);
       }
     }
     // ---- session end: every role has finished its tiles --------------------
@@ -477,14 +651,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   if (tid == 0 && *abort_flag) atomicOr(a.status, kStatusTimeout);
 }
 
-// Packs, per weight set, the layer-2 B operand (FP16, canonical K-major) and
-// the FP32 vectors the epilogue needs: b2[NP], the output weights as pairs
+// Packs, per weight set, the layer-2 B operand (FP16, canonical K-major,
+// K = NP + 16: W2, then b2 as the row met by the constant A block) and the
+// FP32 vectors the epilogue needs: b2[NP], the output weights as pairs
 // {W3[j][0], W3[j+1][0], W3[j][1], W3[j+1][1]} for even j, and b3[2]; padded
 // hidden units get zeros.
 template <int NP>
 __global__ void k_pack_tc(const float* weights, int hp, int set_size, int n_sets, uint8_t* out) {
   using G = Geom<NP>;
-  const int per = NP * NP + 3 * NP + 4;
+  const int per = NP * G::K2 + 3 * NP + 4;
   const int64_t total = (int64_t)n_sets * per;
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
        x += (int64_t)gridDim.x * blockDim.x) {
@@ -492,13 +667,15 @@ __global__ void k_pack_tc(const float* weights, int hp, int set_size, int n_sets
     int r = (int)(x - (int64_t)s * per);
     const float* W = weights + (int64_t)s * set_size;
     uint8_t* base = out + (int64_t)s * G::Set;
-    if (r < NP * NP) {                        // B2[n][k] = W2[k][n]
-      const int n = r / NP, k = r % NP;
-      const float v = (n < hp && k < hp) ? W[w_off_W2(hp) + k * hp + n] : 0.f;
-      reinterpret_cast<__half*>(base)[f16_off(n, k, NP)] = __float2half_rn(v);
+    if (r < NP * G::K2) {                     // B2[n][k] = W2[k][n], B2[n][NP] = b2[n]
+      const int n = r / G::K2, k = r % G::K2;
+      float v = 0.f;
+      if (n < hp && k < hp) v = W[w_off_W2(hp) + k * hp + n];
+      else if (n < hp && k == NP) v = W[w_off_b2(hp) + n];
+      reinterpret_cast<__half*>(base)[f16_off(n, k, G::K2)] = __float2half_rn(v);
       continue;
     }
-    r -= NP * NP;
+    r -= NP * G::K2;
     float v = 0.f;
     if (r < NP) {                             // b2
       v = r < hp ? W[w_off_b2(hp) + r] : 0.f;

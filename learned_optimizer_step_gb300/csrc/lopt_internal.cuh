@@ -103,7 +103,14 @@ struct StepArgs {
 __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
 __device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
 __device__ __forceinline__ float ffma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
-__device__ __forceinline__ float frsqrt(float a) { return rsqrtf(a); }
+// Reciprocal square root: the PTX rsqrt.approx instruction (relative error
+// below 2^-22.9).  Every argument here is at least kEps = 1e-30, a normal
+// number, so flushing subnormals never applies.
+__device__ __forceinline__ float frsqrt(float a) {
+  float r;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+  return r;
+}
 
 // Per-row quantities of the factored second moment for one element.
 struct RowTerms {
