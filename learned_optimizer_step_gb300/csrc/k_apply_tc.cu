@@ -10,38 +10,36 @@
 //
 // One persistent CTA per SM, warp-specialised, linked by mbarriers:
 //   warp 16      producer: bulk-copies (cp.async.bulk, one array per lane) p,
-//                g, m0..2, v of up to 8 tiles of a work unit into a ring of
-//                shared-memory stages, and writes p, m0..2, v of a stage back
-//                with bulk copies once every thread has left it;
-//   warps 8-15   two feature warpgroups (alternate tiles): EMA update,
-//                features, normalisation, FP16 A operand of layer 1 into the
-//                tile slot's tensor memory; the updated m and v go back into
-//                the stage;
+//                g, m0..2, v of up to 8 tiles (a stage) of a work unit into a
+//                ring of shared-memory stages, and writes p, m0..2, v of a
+//                stage back with bulk copies once its two owners are done;
+//   warps 8-15   two feature warpgroups, owning alternate stages: EMA
+//                update, features, normalisation, FP16 A operand of layer 1
+//                into the tile slot's tensor memory; the updated m and v go
+//                back into the stage;
 //   warp 17      MMA issuer (one thread);
-//   warps 0-7    two epilogue warpgroups (alternate tiles): ReLU + FP16 A
-//                operand of layer 2 (in tensor memory) and the b2 preset of
-//                its accumulator; then ReLU(h2), the two-unit output layer
-//                in FP32 on the CUDA cores, and the update of p in the stage.
+//   warps 0-7    two epilogue warpgroups, owning alternate stages: for each
+//                tile ReLU + FP16 A operand of layer 2 (in tensor memory) and
+//                the b2 preset of its accumulator; then for each tile
+//                ReLU(h2), the two-unit output layer in FP32 on the CUDA
+//                cores, and the update of p in the stage.
 // A tile is 128 consecutive elements of one tensor (one per TMEM lane).  A
 // tile slot is a set of tensor-memory columns: the FP32 accumulator (NP
 // columns) and the FP16 A operand of the next MMA (16 columns); the A
 // operands never pass through shared memory.  Per-tensor data (scales,
 // 1/rho, row/column accumulator addresses) travel with each stage in a
-// small record, so the feature warps keep no per-tensor state.
+// small record, so the feature warps keep no per-tensor state.  Owning whole
+// stages keeps the per-tile control flow of the warps small.
 //
-// Small MMAs (M=128, N<=32) cost about 40-50 cycles of the SM's MMA pipe
-// each, whatever their K, and an MMA's result reaches a waiting thread about
-// a thousand cycles after issue.  So a tile uses few MMAs (FP16 operands,
-// K = 32 for layer 1 with b1 against a constant 1 in the A operand, and
-// K = NP + 16 for layer 2 whose last K-step multiplies a constant tensor-
-// memory block (1, 0, ...) with the b2 row of B: 5 MMAs at NP = 32, one
-// tcgen05.commit per issue iteration) and only two MMA round trips: the
-// output layer (two units) runs on the CUDA cores.
-// Stages of different tiles overlap with fixed lags chosen for the largest
-// slack around that latency: in iteration k the MMA thread issues layer 1 of
-// tile k and layer 2 of tile k-5 (K-steps interleaved), then commits once;
-// in step m an epilogue group finishes layer 1 of tile m-4 and the rest of
-// tile m-8.  At most 9 tiles are in flight (10 slots at NP = 32).
+// Small MMAs (M=128, N<=32) cost about 50 cycles of the SM's MMA pipe each,
+// whatever their K, and a few hundred cycles pass from issue to a waiting
+// thread.  So a tile uses few MMAs (FP16 operands, K = 32 for layer 1 with b1
+// against a constant 1 in the A operand, K = NP for layer 2 onto the preset
+// b2: 4 MMAs at NP = 32, one tcgen05.commit per issue iteration) and only two
+// MMA round trips: the output layer (two units) runs on the CUDA cores.  In
+// iteration k the MMA thread issues layer 1 of tile k and layer 2 of tile
+// k-5 (K-steps interleaved), then commits once.  At most S tiles are in
+// flight (10 slots at NP = 32).
 //
 // The tiles of a CTA are processed in sessions: maximal runs of tiles whose
 // tensors share one MLP weight set.  Between sessions the pipeline drains,
@@ -66,10 +64,13 @@ constexpr int kStageElems = kStageTiles * kTile;
 constexpr int kArrays = 6;                // p, g, m0, m1, m2, v
 constexpr int kRingStages = 6;            // stages held in shared memory
 constexpr int kStageBytes = kArrays * kStageElems * 4;
-constexpr int kStageUsers = 4 * kTile;    // feature and epilogue threads, one arrival each per stage
-constexpr int kDone = 8;                  // commit barriers (one per MMA iteration)
+constexpr int kStageUsers = 2 * kTile;    // the feature and the epilogue group that own a stage
+// Commit barriers, one per MMA iteration in rotation.  A thread waiting for
+// iteration j has not yet freed the slot of its tile, so the MMA thread
+// cannot commit iteration j + S; with at least S barriers a waiter never
+// sees its barrier lapped.
+constexpr int kDone = 16;
 constexpr int kLag2 = 5;                  // MMA iteration k: layer 2 of tile k-5
-constexpr int kE1 = 4, kE2 = 8;           // epilogue step m: tiles m-4, m-8
 constexpr int kProducerWarp = 16, kMmaWarp = 17;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -106,14 +107,11 @@ template <int NP>
 struct Geom {
   static constexpr int ACols = 16;                     // A operand: 32 FP16 per row
   static constexpr int SlotCols = NP + ACols;          // accumulator + A operand
-  static constexpr int OneCols = 8;                    // constant A block (1, 0, ..., 0) for b2
-  static constexpr int S = (512 - OneCols) / SlotCols < 16 ? (512 - OneCols) / SlotCols : 16;   // tiles in flight
-  static constexpr int OneCol = S * SlotCols;          // its first column
-  static constexpr int K2 = NP + 16;                   // layer 2: h1 (NP) then the bias block (16)
+  static constexpr int S = 512 / SlotCols < 16 ? 512 / SlotCols : 16;   // tiles in flight
   static constexpr int SBO1 = 32 * 16;                 // layer-1 B operand: K = 32
-  static constexpr int SBO = K2 * 16;                  // layer-2 B operand: K = K2
+  static constexpr int SBO = NP * 16;                  // layer-2 B operand: K = NP
   static constexpr int B1 = NP * 32 * 2;
-  static constexpr int B2 = NP * K2 * 2;
+  static constexpr int B2 = NP * NP * 2;
   static constexpr int Aux = (3 * NP + 4) * 4;         // b2[NP], W3 pairs[NP][2], b3[2], pad
   static constexpr int Set = (B2 + Aux + 1023) / 1024 * 1024;   // packed per-set stride
   static constexpr int oRing = 0;
@@ -127,47 +125,49 @@ struct Geom {
   static constexpr int TmemCols = 512;
   static constexpr uint32_t ID12 = instr_desc(0, 128, NP);
   static_assert(Smem <= 232448, "shared memory of one CTA");
-  static_assert(OneCol + OneCols <= 512 && S > kE2, "tensor memory columns / pipeline depth");
+  // an epilogue group finishes layer 1 of all tiles of a stage before the
+  // rest of any: the stage's last tile must not wait for a slot of its own
+  static_assert(S * SlotCols <= 512 && S >= kStageTiles && S > kLag2 && kDone >= S,
+                "tensor memory columns / pipeline depth");
   static_assert(oRec % 16 == 0 && sizeof(StageRec) % 16 == 0, "16-byte aligned stage records");
 };
 
-// Walks the tiles of a session in order (work units [u, u1), 128-element
-// tiles each) and tracks the ring slot and round parity of each tile's stage.
-// A stage holds up to kStageTiles consecutive tiles of one work unit.
-struct Walk {
+// Walks the stages of a session in order.  A stage holds up to kStageTiles
+// consecutive tiles of one work unit; stage n of a session lives in ring
+// slot n % kRingStages, round n / kRingStages.
+struct StageIter {
   const Unit* units;
   const TensorDesc* desc;
   int32_t u, u1;
-  int32_t tensor;
-  int32_t off, len;   // tile offset in its unit, unit length (elements)
-  int64_t base;       // first element of the unit
-  int32_t st;         // ring slot of the tile's stage
-  uint32_t ph;        // parity of the slot's round
+  int32_t soff, ulen;   // the stage's offset in its unit, the unit's length (elements)
+  int32_t n;            // elements in the stage
+  int32_t k0;           // its first tile, counted in the session
+  int32_t st;           // ring slot
+  uint32_t ph;          // round parity of the slot
   __device__ void init(const Unit* un, const TensorDesc* de, int32_t b, int32_t e) {
-    units = un; desc = de; u = b; u1 = e; st = 0; ph = 0;
-    load();
+    units = un; desc = de; u = b; u1 = e; k0 = 0; st = 0; ph = 0;
+    load_unit();
   }
-  __device__ void load() {
+  __device__ void load_unit() {
     if (u < u1) {
       const Unit x = units[u];
-      tensor = x.tensor;
-      base = (int64_t)x.local * kApplyChunk;
-      len = (int32_t)min(desc[tensor].N - base, (int64_t)kApplyChunk);
-      off = 0;
+      const int64_t base = (int64_t)x.local * kApplyChunk;
+      ulen = (int32_t)min(desc[x.tensor].N - base, (int64_t)kApplyChunk);
+      soff = 0;
+      n = min(ulen, kStageElems);
     }
   }
-  // Moves to the next tile; true when it opens a new stage (st and ph then
-  // describe the new stage).
-  __device__ bool next() {
-    off += kTile;
-    if (off >= len) {
-      if (++u >= u1) return false;
-      load();
-    } else if (off & (kStageElems - 1)) {
-      return false;
+  __device__ bool valid() const { return u < u1; }
+  __device__ void next() {
+    k0 += (n + kTile - 1) / kTile;
+    soff += kStageElems;
+    if (soff >= ulen) {
+      ++u;
+      load_unit();
+    } else {
+      n = min(ulen - soff, kStageElems);
     }
     if (++st == kRingStages) { st = 0; ph ^= 1u; }
-    return true;
   }
 };
 
@@ -186,18 +186,6 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint6
     if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return;
     if (global_ns() - t0 > limit_ns) return;
   }
-}
-
-// A feature or epilogue thread is done with the stage in slot st (round
-// parity ph).  It first waits until that stage has been loaded, so that the
-// slot has left its previous round, then makes its shared-memory writes
-// visible to the bulk copies and arrives.
-__device__ __forceinline__ bool leave_stage(uint64_t* ring_full, uint64_t* stage_done, int st, uint32_t ph,
-                                            volatile int* abort_flag) {
-  if (!mbar_wait_or_abort(ring_full + st, ph, kWaitNs, abort_flag)) return false;
-  fence_proxy_async();
-  mbar_arrive(stage_done + st);
-  return true;
 }
 
 // ReLU + FP16 of one accumulator row, packed two per 32-bit column (16
@@ -247,12 +235,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (warp < 4) {   // the constant A block of layer 2's bias K-step: 1.0h, then zeros
-    uint32_t one[8] = {0x00003C00u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    tmem_st8(tmem + ((uint32_t)(warp * 32) << 16) + G::OneCol, one);
-    tmem_wait_st();
-  }
-  tc_fence_before();
 
   const int32_t U = a.n_units;
   const int32_t u_first = (int32_t)((int64_t)blockIdx.x * U / gridDim.x);
@@ -369,108 +351,95 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       bulk_wait_all();   // every write-back complete before the session ends
     } else if (warp >= 8 && warp < 16) {
       // --------------------------- feature warpgroups ------------------------
-      // Group grp takes the tiles k with k % 2 == grp.  Every thread walks
-      // all tiles so that it leaves each stage exactly once.
+      // Group grp owns the stages n with n % 2 == grp and builds the A
+      // operand of layer 1 for each of their tiles in order.
       const int grp = (warp - 8) >> 2;
       const int t = tid - 256 - 128 * grp;
       const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      Walk w;
-      w.init(a.units, a.desc, u0, u1);
-      int s = grp;          // slot of this group's next tile
-      uint32_t sph = 0;     // its round parity
+      StageIter si;
+      si.init(a.units, a.desc, u0, u1);
       bool ok = true;
-      for (int32_t k = 0; k < K; ++k) {
-        if (k > 0) {
-          const int pst = w.st;
-          const uint32_t pph = w.ph;
-          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) {
-            ok = false;
-            break;
-          }
-        }
-        if ((k & 1) != grp) continue;
-        if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag) ||
-            !mbar_wait_or_abort(ring_full + w.st, w.ph, kWaitNs, abort_flag)) {
-          ok = false;
-          break;
-        }
-        const StageRec& rc = rec[w.st];
+      for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
+        if ((ns & 1) != grp) continue;
+        if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
+        const StageRec& rc = rec[si.st];
         const bool stg = rc.bytes != 0;
-        const int x = (w.off & (kStageElems - 1)) + t;   // element offset in the stage
-        const bool valid = w.off + t < w.len;
-        const int64_t e = rc.e0 + x;
-        float* rs = ring + w.st * (kArrays * kStageElems) + x;
-        float p = 0.f, g = 0.f, m[3] = {0.f, 0.f, 0.f}, v = 0.f;
-        float c[3] = {0.f, 0.f, 0.f};
-        float r[3] = {0.f, 0.f, 0.f};
-        if (valid) {
-          if (stg) {
-            p = rs[0]; g = rs[kStageElems]; m[0] = rs[2 * kStageElems]; m[1] = rs[3 * kStageElems];
-            m[2] = rs[4 * kStageElems]; v = rs[5 * kStageElems];
+        float* const sbase = ring + si.st * (kArrays * kStageElems);
+        const int ntl = (si.n + kTile - 1) / kTile;
+        int s = si.k0 % S;                          // slot of the stage's first tile
+        uint32_t sph = (uint32_t)((si.k0 / S) & 1);  // its round parity
+        for (int j = 0; j < ntl; ++j) {
+          if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) { ok = false; break; }
+          const int x = j * kTile + t;                 // element offset in the stage
+          const int xi = min(x, si.n - 1);             // past the end: index math of the last element
+          float p, g, m[3], v;
+          if (stg) {   // elements past the end read and write unused stage words
+            p = sbase[x]; g = sbase[kStageElems + x]; m[0] = sbase[2 * kStageElems + x];
+            m[1] = sbase[3 * kStageElems + x]; m[2] = sbase[4 * kStageElems + x]; v = sbase[5 * kStageElems + x];
           } else {
             const TensorDesc& d = a.desc[rc.tensor];
+            const int64_t e = rc.e0 + xi;
             p = d.p[e]; g = __ldg(d.g + e); v = d.v[e];
 #pragma unroll
             for (int q = 0; q < 3; ++q) m[q] = d.m[q][e];
           }
-          // row and column of the element
-          // j0 + x < C + kStageElems, so a float quotient is exact to within one
+          // row and column of the element: j0 + xi < C + kStageElems, so a
+          // float quotient is exact to within one
           const uint32_t C = (uint32_t)rc.C;
           int64_t i = rc.i0;
-          uint32_t j = (uint32_t)rc.j0 + (uint32_t)x;
-          if (j >= C) {
-            uint32_t q = (uint32_t)((float)j * rc.invC);
-            int32_t rem = (int32_t)(j - q * C);
+          uint32_t jc = (uint32_t)rc.j0 + (uint32_t)xi;
+          if (jc >= C) {
+            uint32_t q = (uint32_t)((float)jc * rc.invC);
+            int32_t rem = (int32_t)(jc - q * C);
             if (rem < 0) { --q; rem += (int32_t)C; }
             else if (rem >= (int32_t)C) { ++q; rem -= (int32_t)C; }
             i += q;
-            j = (uint32_t)rem;
+            jc = (uint32_t)rem;
           }
+          float c[3], r[3];
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
-            c[q] = __ldg(rc.c[q] + j);
+            c[q] = __ldg(rc.c[q] + jc);
             r[q] = __ldg(rc.r[q] + i);
           }
-        }
-        float inv_rho[3];
+          float inv_rho[3];
 #pragma unroll
-        for (int q = 0; q < 3; ++q) inv_rho[q] = rc.inv_rho[q];
-        const RowTerms rt = row_terms_of(r, inv_rho);
-        float f[kStats];
-        lopt_features(p, g, m, v, rt, c, f);
-        if (valid) {
+          for (int q = 0; q < 3; ++q) inv_rho[q] = rc.inv_rho[q];
+          const RowTerms rt = row_terms_of(r, inv_rho);
+          float f[kStats];
+          lopt_features(p, g, m, v, rt, c, f);
           if (stg) {
-            rs[2 * kStageElems] = m[0]; rs[3 * kStageElems] = m[1]; rs[4 * kStageElems] = m[2];
-            rs[5 * kStageElems] = v;
-          } else {
+            sbase[2 * kStageElems + x] = m[0]; sbase[3 * kStageElems + x] = m[1];
+            sbase[4 * kStageElems + x] = m[2]; sbase[5 * kStageElems + x] = v;
+          } else if (x < si.n) {
             const TensorDesc& d = a.desc[rc.tensor];
+            const int64_t e = rc.e0 + x;
 #pragma unroll
             for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
             d.v[e] = v;
           }
-        }
-        // normalised features, FP16, into this lane's row of the slot's A
-        // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
-        uint32_t av[16];
-        const float4* sc4 = reinterpret_cast<const float4*>(rc.sc);
+          // normalised features, FP16, into this lane's row of the slot's A
+          // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
+          uint32_t av[16];
+          const float4* sc4 = reinterpret_cast<const float4*>(rc.sc);
 #pragma unroll
-        for (int q = 0; q < 7; ++q) {
-          const float4 sq = sc4[q];
-          const float2 lo = __fmul2_rn(make_float2(f[4 * q], f[4 * q + 1]), make_float2(sq.x, sq.y));
-          const float2 hi = __fmul2_rn(make_float2(f[4 * q + 2], f[4 * q + 3]), make_float2(sq.z, sq.w));
-          av[2 * q] = f16x2(lo.x, lo.y);
-          av[2 * q + 1] = f16x2(hi.x, hi.y);
+          for (int q = 0; q < 7; ++q) {
+            const float4 sq = sc4[q];
+            av[2 * q] = f16x2(f[4 * q] * sq.x, f[4 * q + 1] * sq.y);
+            av[2 * q + 1] = f16x2(f[4 * q + 2] * sq.z, f[4 * q + 3] * sq.w);
+          }
+          av[14] = 0x00003C00u;   // 1.0h, 0
+          av[15] = 0u;
+          tmem_st16(t_lane + s * G::SlotCols + NP, av);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(a1_full + s);
+          if (++s == S) { s = 0; sph ^= 1u; }
         }
-        av[14] = 0x00003C00u;   // 1.0h, 0
-        av[15] = 0u;
-        tmem_st16(t_lane + s * G::SlotCols + NP, av);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(a1_full + s);
-        s += 2;
-        if (s >= S) { s -= S; sph ^= 1u; }
+        if (!ok) break;
+        fence_proxy_async();   // m, v in the stage, before its write-back
+        mbar_arrive(stage_done + si.st);
       }
-      if (ok && K > 0) leave_stage(ring_full, stage_done, w.st, w.ph, abort_flag);
     } else if (warp == kMmaWarp) {
       // ------------------------------- MMA issuer ----------------------------
       if (lane == 0) {
@@ -504,9 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       }
     } else if (warp < 8) {
       // ------------------------------ epilogue -------------------------------
-      // Group h takes the steps m with m % 2 == h.  Step m finishes layer 1
-      // of tile t1 = m-4 (ReLU, FP16 A operand of layer 2), then the rest of
-      // tile t2 = m-8 (ReLU(h2), output layer, update of p).
+      // Group h owns the stages n with n % 2 == h.  For a stage it first
+      // finishes layer 1 of every tile (ReLU, FP16 A operand of layer 2, b2
+      // preset of its accumulator), then the rest of every tile (ReLU(h2),
+      // output layer, update of p in the stage).
       const int h = warp >> 2;
       const int t = tid - 128 * h;
       const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -514,29 +484,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
       const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
       const float lr = a.lr;
-      Walk w;   // at tile wk; the stages behind it have been left
-      w.init(a.units, a.desc, u0, u1);
-      int32_t wk = 0;
+      StageIter si;
+      si.init(a.units, a.desc, u0, u1);
       bool ok = true;
-      for (int32_t m = h; m - kE2 < K; m += 2) {
-        if (*abort_flag) { ok = false; break; }
-        const int32_t t1 = m - kE1, t2 = m - kE2;
-        const bool e1 = t1 >= 0 && t1 < K, e2 = t2 >= 0;
-        const int s1 = e1 ? t1 % S : 0, s2 = e2 ? t2 % S : 0;
-        while (e2 && wk < t2) {
-          ++wk;
-          const int pst = w.st;
-          const uint32_t pph = w.ph;
-          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) { ok = false; break; }
-        }
-        if (!ok) break;
-        if (e1) {   // layer 1 of tile t1: FP16 A operand of layer 2
-          if (!mbar_wait_or_abort(done + (t1 & (kDone - 1)), (uint32_t)((t1 / kDone) & 1), kWaitNs, abort_flag)) {
+      for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
+        if ((ns & 1) != h) continue;
+        // the stage's record (written by the producer before it was loaded)
+        if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
+        const int ntl = (si.n + kTile - 1) / kTile;
+        const int s0 = si.k0 % S;
+        // ---- layer 1 of every tile
+        int s = s0;
+        for (int j = 0; j < ntl; ++j) {
+          const int32_t k = si.k0 + j;
+          if (!mbar_wait_or_abort(done + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t col = t_lane + s1 * G::SlotCols;
+          const uint32_t col = t_lane + s * G::SlotCols;
           uint32_t av[16];
           {
             uint32_t h1[NP];
@@ -553,85 +519,76 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
           }
           tmem_st_row<NP>(col, b2);
-        }
-        if (e1) {
           tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(a2_full + s1);
+          mbar_arrive(a2_full + s);
+          if (++s == S) s = 0;
         }
-        if (e2) {   // rest of tile t2: its slot is freed as soon as h2 is read
-          const int32_t it = t2 + kLag2;
+        if (!ok) break;
+        // ---- the rest of every tile; a slot is freed as soon as h2 is read
+        const StageRec& rc = rec[si.st];
+        const bool stg = rc.bytes != 0;
+        float* const pst = ring + si.st * (kArrays * kStageElems);
+        s = s0;
+        for (int j = 0; j < ntl; ++j) {
+          const int32_t it = si.k0 + j + kLag2;
           if (!mbar_wait_or_abort(done + (it & (kDone - 1)), (uint32_t)((it / kDone) & 1), kWaitNs, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           uint32_t h2[NP];
-          tmem_ld_row<NP>(t_lane + s2 * G::SlotCols, h2);
+          tmem_ld_row<NP>(t_lane + s * G::SlotCols, h2);
           tmem_wait_ld();
           tc_fence_before();
-          mbar_arrive(slot_empty + s2);
-          if (w.off + t < w.len) {
-            // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3, in
-            // chunks of 8 hidden units whose weights are loaded one chunk
-            // ahead (shared-memory latency off the FMA chains)
-            constexpr int kCh = NP / 8;
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};   // (o0, o1) x 2 chains
-            float4 wcur[4], wnext[4];
+          mbar_arrive(slot_empty + s);
+          if (++s == S) s = 0;
+          // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3, in
+          // chunks of 8 hidden units whose weights are loaded one chunk
+          // ahead (shared-memory latency off the FMA chains)
+          constexpr int kCh = NP / 8;
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                           make_float2(0.f, 0.f)};   // (o0, o1) x 2 chains
+          float4 wcur[4], wnext[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) wcur[q] = w3[q];
+          for (int q = 0; q < 4; ++q) wcur[q] = w3[q];
 #pragma unroll
-            for (int ch = 0; ch < kCh; ++ch) {
-              if (ch + 1 < kCh) {
+          for (int ch = 0; ch < kCh; ++ch) {
+            if (ch + 1 < kCh) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) wnext[q] = w3[4 * (ch + 1) + q];
-              }
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int u = 8 * ch + 2 * q;
-                const float2 hr = make_float2(fmaxf(__uint_as_float(h2[u]), 0.f),
-                                              fmaxf(__uint_as_float(h2[u + 1]), 0.f));
-                acc[(q & 1) * 2] = __ffma2_rn(hr, make_float2(wcur[q].x, wcur[q].y), acc[(q & 1) * 2]);
-                acc[(q & 1) * 2 + 1] = __ffma2_rn(hr, make_float2(wcur[q].z, wcur[q].w), acc[(q & 1) * 2 + 1]);
-              }
-              if (ch + 1 < kCh) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) wcur[q] = wnext[q];
-              }
+              for (int q = 0; q < 4; ++q) wnext[q] = w3[4 * (ch + 1) + q];
             }
-            const float o0 = (acc[0].x + acc[0].y) + (acc[2].x + acc[2].y) + b30;
-            const float o1 = (acc[1].x + acc[1].y) + (acc[3].x + acc[3].y) + b31;
-            // exp(x) = 2^(x log2 e) with the PTX ex2.approx instruction
-            // (relative error below 2^-22); here |x| = |o1| * 1e-3 is small
-            float ex;
-            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
-            const float upd = o0 * ex * kOutScale;
-            const StageRec& rc = rec[w.st];
-            if (rc.bytes != 0) {
-              float* pp = ring + w.st * (kArrays * kStageElems) + (w.off & (kStageElems - 1)) + t;
-              *pp = *pp - lr * upd;
-            } else {
-              float* pp = a.desc[rc.tensor].p + (w.base + w.off + t);
-              *pp = *pp - lr * upd;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int u = 8 * ch + 2 * q;
+              const float2 hr = make_float2(fmaxf(__uint_as_float(h2[u]), 0.f),
+                                            fmaxf(__uint_as_float(h2[u + 1]), 0.f));
+              acc[(q & 1) * 2] = __ffma2_rn(hr, make_float2(wcur[q].x, wcur[q].y), acc[(q & 1) * 2]);
+              acc[(q & 1) * 2 + 1] = __ffma2_rn(hr, make_float2(wcur[q].z, wcur[q].w), acc[(q & 1) * 2 + 1]);
+            }
+            if (ch + 1 < kCh) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) wcur[q] = wnext[q];
             }
           }
+          const float o0 = (acc[0].x + acc[0].y) + (acc[2].x + acc[2].y) + b30;
+          const float o1 = (acc[1].x + acc[1].y) + (acc[3].x + acc[3].y) + b31;
+          // exp(x) = 2^(x log2 e) with the PTX ex2.approx instruction
+          // (relative error below 2^-22); here |x| = |o1| * 1e-3 is small
+          float ex;
+          asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
+          const float upd = o0 * ex * kOutScale;
+          const int x = j * kTile + t;
+          if (stg) {   // past the end: an unused stage word
+            pst[x] = pst[x] - lr * upd;
+          } else if (x < si.n) {
+            float* pp = a.desc[rc.tensor].p + (rc.e0 + x);
+            *pp = *pp - lr * upd;
+          }
         }
-        if (e2 && wk + 1 < K) {   // leave t2's stage as soon as the next tile opens another one
-          ++wk;
-          const int pst = w.st;
-          const uint32_t pph = w.ph;
-          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) { ok = false; break; }
-        }
-      }
-      if (ok && K > 0) {
-        while (ok && wk < K - 1) {
-          ++wk;
-          const int pst = w.st;
-          const uint32_t pph = w.ph;
-          if (w.next() && !leave_stage(ring_full, stage_done, pst, pph, abort_flag)) ok = false;
-        }
-        if (ok) leave_stage(ring_full, stage_done, w.st, w.ph, abort_flag);
+        if (!ok) break;
+        fence_proxy_async();   // p in the stage, before its write-back
+        mbar_arrive(stage_done + si.st);
       }
     }
     // ---- session end: every role has finished its tiles --------------------
@@ -651,15 +608,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   if (tid == 0 && *abort_flag) atomicOr(a.status, kStatusTimeout);
 }
 
-// Packs, per weight set, the layer-2 B operand (FP16, canonical K-major,
-// K = NP + 16: W2, then b2 as the row met by the constant A block) and the
-// FP32 vectors the epilogue needs: b2[NP], the output weights as pairs
+// Packs, per weight set, the layer-2 B operand (FP16, canonical K-major) and
+// the FP32 vectors the epilogue needs: b2[NP], the output weights as pairs
 // {W3[j][0], W3[j+1][0], W3[j][1], W3[j+1][1]} for even j, and b3[2]; padded
 // hidden units get zeros.
 template <int NP>
 __global__ void k_pack_tc(const float* weights, int hp, int set_size, int n_sets, uint8_t* out) {
   using G = Geom<NP>;
-  const int per = NP * G::K2 + 3 * NP + 4;
+  const int per = NP * NP + 3 * NP + 4;
   const int64_t total = (int64_t)n_sets * per;
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
        x += (int64_t)gridDim.x * blockDim.x) {
@@ -667,15 +623,13 @@ __global__ void k_pack_tc(const float* weights, int hp, int set_size, int n_sets
     int r = (int)(x - (int64_t)s * per);
     const float* W = weights + (int64_t)s * set_size;
     uint8_t* base = out + (int64_t)s * G::Set;
-    if (r < NP * G::K2) {                     // B2[n][k] = W2[k][n], B2[n][NP] = b2[n]
-      const int n = r / G::K2, k = r % G::K2;
-      float v = 0.f;
-      if (n < hp && k < hp) v = W[w_off_W2(hp) + k * hp + n];
-      else if (n < hp && k == NP) v = W[w_off_b2(hp) + n];
-      reinterpret_cast<__half*>(base)[f16_off(n, k, G::K2)] = __float2half_rn(v);
+    if (r < NP * NP) {                        // B2[n][k] = W2[k][n]
+      const int n = r / NP, k = r % NP;
+      const float v = (n < hp && k < hp) ? W[w_off_W2(hp) + k * hp + n] : 0.f;
+      reinterpret_cast<__half*>(base)[f16_off(n, k, NP)] = __float2half_rn(v);
       continue;
     }
-    r -= NP * G::K2;
+    r -= NP * NP;
     float v = 0.f;
     if (r < NP) {                             // b2
       v = r < hp ? W[w_off_b2(hp) + r] : 0.f;
