@@ -17,7 +17,7 @@
 //                update, features, normalisation, FP16 A operand of layer 1
 //                into the tile slot's tensor memory; the updated m and v go
 //                back into the stage;
-//   warp 17      MMA issuer (one thread);
+//   warps 17-18  MMA issuers, one thread each: layer 1 and layer 2;
 //   warps 0-7    two epilogue warpgroups, owning alternate stages: for each
 //                tile ReLU + FP16 A operand of layer 2 (in tensor memory) and
 //                the b2 preset of its accumulator; then for each tile
@@ -35,11 +35,11 @@
 // whatever their K, and a few hundred cycles pass from issue to a waiting
 // thread.  So a tile uses few MMAs (FP16 operands, K = 32 for layer 1 with b1
 // against a constant 1 in the A operand, K = NP for layer 2 onto the preset
-// b2: 4 MMAs at NP = 32, one tcgen05.commit per issue iteration) and only two
-// MMA round trips: the output layer (two units) runs on the CUDA cores.  In
-// iteration k the MMA thread issues layer 1 of tile k and layer 2 of tile
-// k-5 (K-steps interleaved), then commits once.  At most S tiles are in
-// flight (10 slots at NP = 32).
+// b2: 4 MMAs at NP = 32, one tcgen05.commit per layer and tile) and only two
+// MMA round trips: the output layer (two units) runs on the CUDA cores.  The
+// two layers are issued by two threads in different warps, so that issuing
+// (a few dozen instructions per tile) is spread over two schedulers.  At
+// most S tiles are in flight (10 slots at NP = 32).
 //
 // The tiles of a CTA are processed in sessions: maximal runs of tiles whose
 // tensors share one MLP weight set.  Between sessions the pipeline drains,
@@ -58,20 +58,19 @@ namespace lopt {
 namespace {
 
 constexpr int kTile = 128;                // elements per tile (= TMEM lanes)
-constexpr int kThreads = 18 * 32;         // 8 epilogue + 8 feature + producer + MMA warps
+constexpr int kThreads = 19 * 32;         // 8 epilogue + 8 feature + producer + 2 MMA warps
 constexpr int kStageTiles = 8;            // tiles per stage (4 KB per array)
 constexpr int kStageElems = kStageTiles * kTile;
 constexpr int kArrays = 6;                // p, g, m0, m1, m2, v
 constexpr int kRingStages = 6;            // stages held in shared memory
 constexpr int kStageBytes = kArrays * kStageElems * 4;
 constexpr int kStageUsers = 2 * kTile;    // the feature and the epilogue group that own a stage
-// Commit barriers, one per MMA iteration in rotation.  A thread waiting for
-// iteration j has not yet freed the slot of its tile, so the MMA thread
-// cannot commit iteration j + S; with at least S barriers a waiter never
-// sees its barrier lapped.
+// Commit barriers per layer, one per tile in rotation.  A thread waiting for
+// tile j has not yet freed the slot of its tile, so no MMA thread can commit
+// tile j + S; with at least S barriers a waiter never sees its barrier
+// lapped.
 constexpr int kDone = 16;
-constexpr int kLag2 = 5;                  // MMA iteration k: layer 2 of tile k-5
-constexpr int kProducerWarp = 16, kMmaWarp = 17;
+constexpr int kProducerWarp = 16, kMma1Warp = 17, kMma2Warp = 18;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // Where stage array q (p, g, m0, m1, m2, v) of a tensor lives.
@@ -118,7 +117,7 @@ struct Geom {
   static constexpr int oB1 = oRing + kRingStages * kStageBytes;
   static constexpr int oB2 = oB1 + B1;                  // B2, b2, W3, b3 as packed
   static constexpr int oBar = (oB2 + Set + 15) / 16 * 16;
-  static constexpr int nBars = 2 * kRingStages + 3 * S + kDone;
+  static constexpr int nBars = 2 * kRingStages + 3 * S + 2 * kDone;
   static constexpr int oRec = (oBar + nBars * 8 + 15) / 16 * 16;   // records are read as float4
   static constexpr int oInfo = oRec + kRingStages * (int)sizeof(StageRec);
   static constexpr int Smem = oInfo + 64;
@@ -127,7 +126,7 @@ struct Geom {
   static_assert(Smem <= 232448, "shared memory of one CTA");
   // an epilogue group finishes layer 1 of all tiles of a stage before the
   // rest of any: the stage's last tile must not wait for a slot of its own
-  static_assert(S * SlotCols <= 512 && S >= kStageTiles && S > kLag2 && kDone >= S,
+  static_assert(S * SlotCols <= 512 && S >= kStageTiles && kDone >= S,
                 "tensor memory columns / pipeline depth");
   static_assert(oRec % 16 == 0 && sizeof(StageRec) % 16 == 0, "16-byte aligned stage records");
 };
@@ -220,7 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   uint64_t* a1_full = stage_done + R;
   uint64_t* a2_full = a1_full + S;
   uint64_t* slot_empty = a2_full + S;
-  uint64_t* done = slot_empty + S;
+  uint64_t* done1 = slot_empty + S;
+  uint64_t* done2 = done1 + kDone;
   StageRec* rec = reinterpret_cast<StageRec*>(smem + G::oRec);
   int32_t* info = reinterpret_cast<int32_t*>(smem + G::oInfo);   // session: end unit, tiles
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + G::oInfo + 32);
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
         mbar_init(a2_full + s, kTile);
         mbar_init(slot_empty + s, kTile);
       }
-      for (int s = 0; s < kDone; ++s) mbar_init(done + s, 1);
+      for (int s = 0; s < 2 * kDone; ++s) mbar_init(done1 + s, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     {  // weights of the session's set: layer-1 operand of its first tensor,
@@ -440,36 +440,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
         fence_proxy_async();   // m, v in the stage, before its write-back
         mbar_arrive(stage_done + si.st);
       }
-    } else if (warp == kMmaWarp) {
-      // ------------------------------- MMA issuer ----------------------------
+    } else if (warp == kMma1Warp || warp == kMma2Warp) {
+      // ------------------------------ MMA issuers ----------------------------
+      // One thread per layer: layer 1 of tile k once its A operand is in
+      // tensor memory, committed to done1[k]; layer 2 of tile k once its A
+      // operand and b2 preset are, committed to done2[k].
       if (lane == 0) {
-        const uint64_t dB1 = smem_desc(s_base + G::oB1, 128, G::SBO1);
-        const uint64_t dB2 = smem_desc(s_base + G::oB2, 128, G::SBO);
-        const int k_end = K + kLag2;
-        // slot index and phase of tile k and of tile k - kLag2, kept incrementally
-        int s1 = 0, s2 = S - kLag2;
-        uint32_t p1 = 0, p2 = 1;
+        const bool l1 = warp == kMma1Warp;
+        const uint64_t dB = l1 ? smem_desc(s_base + G::oB1, 128, G::SBO1) : smem_desc(s_base + G::oB2, 128, G::SBO);
+        uint64_t* const full = l1 ? a1_full : a2_full;
+        uint64_t* const fin = l1 ? done1 : done2;
+        const int ksteps = l1 ? 2 : NP / 16;   // K-steps of 16 FP16 values (8 A columns)
+        int s = 0;
+        uint32_t ph = 0;
         int k = 0;
-        for (; k < k_end; ++k) {
-          const bool do1 = k < K;
-          const bool do2 = k >= kLag2;
-          if (do1 && !mbar_wait_or_abort(a1_full + s1, p1, kWaitNs, abort_flag)) break;
-          if (do2 && !mbar_wait_or_abort(a2_full + s2, p2, kWaitNs, abort_flag)) break;
+        for (; k < K; ++k) {
+          if (!mbar_wait_or_abort(full + s, ph, kWaitNs, abort_flag)) break;
           tc_fence_after();
-          const uint32_t d1 = tmem + s1 * G::SlotCols, d2 = tmem + s2 * G::SlotCols;
-          // K-steps of the two layers interleaved (independent accumulators);
-          // one K-step of 16 FP16 values = 8 tensor-memory columns of A
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            if (do1) mma_f16_ts(d1, d1 + NP + 8 * kk, dB1 + 16 * kk, G::ID12, kk > 0);
-            if (do2 && kk < NP / 16) mma_f16_ts(d2, d2 + NP + 8 * kk, dB2 + 16 * kk, G::ID12, 1u);  // onto b2
-          }
-          mma_commit(done + (k % kDone));   // tracks every MMA issued so far
-          if (++s1 == S) { s1 = 0; p1 ^= 1; }
-          if (++s2 == S) { s2 = 0; p2 ^= 1; }
+          const uint32_t d = tmem + s * G::SlotCols;
+          // layer 1 overwrites its accumulator; layer 2 adds onto the b2 preset
+          mma_f16_ts(d, d + NP, dB, G::ID12, l1 ? 0u : 1u);
+          if (ksteps > 1) mma_f16_ts(d, d + NP + 8, dB + 16, G::ID12, 1u);
+          mma_commit(fin + (k & (kDone - 1)));   // tracks every MMA of this thread so far
+          if (++s == S) { s = 0; ph ^= 1u; }
         }
         // nothing of ours may still be running when the session ends
-        if (k > 0) mbar_drain(done + ((k - 1) % kDone), (uint32_t)(((k - 1) / kDone) & 1), kWaitNs / 10);
+        if (k > 0) mbar_drain(fin + ((k - 1) & (kDone - 1)), (uint32_t)(((k - 1) / kDone) & 1), kWaitNs / 10);
       }
     } else if (warp < 8) {
       // ------------------------------ epilogue -------------------------------
@@ -497,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
         int s = s0;
         for (int j = 0; j < ntl; ++j) {
           const int32_t k = si.k0 + j;
-          if (!mbar_wait_or_abort(done + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
+          if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
             ok = false;
             break;
           }
@@ -531,8 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
         float* const pst = ring + si.st * (kArrays * kStageElems);
         s = s0;
         for (int j = 0; j < ntl; ++j) {
-          const int32_t it = si.k0 + j + kLag2;
-          if (!mbar_wait_or_abort(done + (it & (kDone - 1)), (uint32_t)((it / kDone) & 1), kWaitNs, abort_flag)) {
+          const int32_t k = si.k0 + j;
+          if (!mbar_wait_or_abort(done2 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
             ok = false;
             break;
           }
