@@ -281,11 +281,13 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < (1u << 30); ++it) {
-    if (mbar_try_wait_sleep(bar, parity, kSuspendHintNs)) return true;
-    if (*abort) return false;
-    if (global_ns() - t0 > limit_ns) {
-      *abort = 1;
-      return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15) == 15) {
+      if (*abort) return false;
+      if (global_ns() - t0 > limit_ns) {
+        *abort = 1;
+        return false;
+      }
     }
   }
   *abort = 1;
