@@ -96,9 +96,75 @@ __device__ void strip_pass(const TensorDesc& d, int64_t r0, int nrows, float* co
   __syncthreads();
 }
 
+// Row-parallel pass for strips with at least one row per warp: warp w
+// reads rows w, w + 8, ... of the strip, one coalesced row segment of up to
+// 32 * 4 * kColVec columns at a time; a row's sum is one warp reduction
+// added to rowacc by that warp alone, and each lane keeps the column sums
+// of its columns in registers until the warps' column sums are combined in
+// warp order.  Same results in every run: every sum has a fixed order.
+constexpr int kColVec = 8;                 // vectors of W columns per lane and segment
+
+template <int W>
+__device__ void strip_rows_pass(const TensorDesc& d, int64_t r0, int nrows, float* colpart_strip,
+                                float* rowacc, float* colsum) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t C = d.C;
+  constexpr int kSeg = 32 * W * kColVec;   // columns per segment
+  for (int i = tid; i < nrows; i += kT) rowacc[i] = 0.f;
+  __syncthreads();
+  for (int64_t c0 = 0; c0 < C; c0 += kSeg) {
+    float col[kColVec][W];
+#pragma unroll
+    for (int v = 0; v < kColVec; ++v)
+#pragma unroll
+      for (int q = 0; q < W; ++q) col[v][q] = 0.f;
+    for (int row = warp; row < nrows; row += kWarps) {
+      const float* src = d.g + (r0 + row) * C + c0;
+      float rs = 0.f;
+#pragma unroll
+      for (int v = 0; v < kColVec; ++v) {
+        const int64_t j = (int64_t)(v * 32 + lane) * W;   // column offset in the segment
+        if (c0 + j < C) {
+          if constexpr (W == 4) {
+            const float4 x = __ldg(reinterpret_cast<const float4*>(src + j));
+            const float s0 = fmul(x.x, x.x), s1 = fmul(x.y, x.y), s2 = fmul(x.z, x.z), s3 = fmul(x.w, x.w);
+            col[v][0] = fadd(col[v][0], s0);
+            col[v][1] = fadd(col[v][1], s1);
+            col[v][2] = fadd(col[v][2], s2);
+            col[v][3] = fadd(col[v][3], s3);
+            rs = fadd(rs, fadd(fadd(s0, s1), fadd(s2, s3)));
+          } else {
+            const float x = __ldg(src + j);
+            const float s0 = fmul(x, x);
+            col[v][0] = fadd(col[v][0], s0);
+            rs = fadd(rs, s0);
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) rs = fadd(rs, __shfl_xor_sync(0xffffffffu, rs, off));
+      if (lane == 0) rowacc[row] = fadd(rowacc[row], rs);
+    }
+    // this warp's column sums, then the warps' sums in warp order
+#pragma unroll
+    for (int v = 0; v < kColVec; ++v)
+#pragma unroll
+      for (int q = 0; q < W; ++q) colsum[warp * kSeg + (v * 32 + lane) * W + q] = col[v][q];
+    __syncthreads();
+    for (int jj = tid; jj < kSeg && c0 + jj < C; jj += kT) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) s = fadd(s, colsum[w * kSeg + jj]);
+      colpart_strip[c0 + jj] = s;
+    }
+    __syncthreads();
+  }
+}
+
 __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
   __shared__ float rowacc[kMaxStripRows];
   __shared__ float wsum[2][kWarps][kRowBatch];
+  __shared__ __align__(16) float colsum[kWarps * 32 * 4 * kColVec];   // 32 KB
   __shared__ double red[kWarps][3];
   __shared__ int is_last;
 
@@ -109,10 +175,14 @@ __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
   const int nrows = (int)min((int64_t)d.strip_rows, d.R - r0);
   float* colpart_strip = a.colpart + d.colpart_off + (int64_t)u.local * d.C;
 
-  if (d.vec4 && (d.C % 4 == 0))
-    strip_pass<4>(d, r0, nrows, colpart_strip, rowacc, wsum);
-  else
-    strip_pass<1>(d, r0, nrows, colpart_strip, rowacc, wsum);
+  const bool v4 = d.vec4 && (d.C % 4 == 0);
+  if (nrows >= kWarps) {   // a row or more per warp
+    if (v4) strip_rows_pass<4>(d, r0, nrows, colpart_strip, rowacc, colsum);
+    else    strip_rows_pass<1>(d, r0, nrows, colpart_strip, rowacc, colsum);
+  } else {                 // few long rows: all threads across the columns
+    if (v4) strip_pass<4>(d, r0, nrows, colpart_strip, rowacc, wsum);
+    else    strip_pass<1>(d, r0, nrows, colpart_strip, rowacc, wsum);
+  }
 
   // Row means -> row accumulators; partial sums of the new r_k for rho_k.
   double acc[3] = {0.0, 0.0, 0.0};

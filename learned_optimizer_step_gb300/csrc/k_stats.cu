@@ -1,5 +1,5 @@
-// K1: statistics pass -- features built in registers, per-feature sum of
-// squares over each whole tensor.
+// K1: statistics pass -- per-feature sum of squares over each whole tensor,
+// from the squares of the features built in registers.
 //
 // "PyLO: Towards Accessible Learned Optimizers in PyTorch", section
 // "融合カーネル戦略", kernel 1: construct_features() fused with
@@ -42,14 +42,10 @@ constexpr int kWarps = kT / 32;
 __device__ __forceinline__ void accumulate_element(const TensorDesc& d, const float inv_rho[3],
                                                    int64_t e, int64_t i, int64_t j,
                                                    float acc[kStats]) {
-  float m[3] = {__ldg(d.m[0] + e), __ldg(d.m[1] + e), __ldg(d.m[2] + e)};
-  float v = __ldg(d.v + e);
+  const float m[3] = {__ldg(d.m[0] + e), __ldg(d.m[1] + e), __ldg(d.m[2] + e)};
   const float c[3] = {__ldg(d.c[0] + j), __ldg(d.c[1] + j), __ldg(d.c[2] + j)};
-  const RowTerms rt = row_terms(d, inv_rho, i);
-  float f[kStats];
-  lopt_features(__ldg(d.p + e), __ldg(d.g + e), m, v, rt, c, f);
-#pragma unroll
-  for (int q = 0; q < kStats; ++q) acc[q] = ffma(f[q], f[q], acc[q]);
+  const float r[3] = {__ldg(d.r[0] + i), __ldg(d.r[1] + i), __ldg(d.r[2] + i)};
+  lopt_feature_squares(__ldg(d.p + e), __ldg(d.g + e), m, __ldg(d.v + e), r, c, inv_rho, acc);
 }
 
 __global__ void __launch_bounds__(kT) k_stats(StepArgs a) {
@@ -85,7 +81,7 @@ __global__ void __launch_bounds__(kT) k_stats(StepArgs a) {
         const float4 k0 = __ldg(reinterpret_cast<const float4*>(d.c[0] + w.j));
         const float4 k1 = __ldg(reinterpret_cast<const float4*>(d.c[1] + w.j));
         const float4 k2 = __ldg(reinterpret_cast<const float4*>(d.c[2] + w.j));
-        const RowTerms rt = row_terms(d, inv_rho, w.i);
+        const float r[3] = {__ldg(d.r[0] + w.i), __ldg(d.r[1] + w.i), __ldg(d.r[2] + w.i)};
         const float pp[4] = {p4.x, p4.y, p4.z, p4.w}, gg[4] = {g4.x, g4.y, g4.z, g4.w};
         const float m0[4] = {a4.x, a4.y, a4.z, a4.w}, m1[4] = {b4.x, b4.y, b4.z, b4.w};
         const float m2[4] = {c4.x, c4.y, c4.z, c4.w}, vv[4] = {v4.x, v4.y, v4.z, v4.w};
@@ -93,13 +89,9 @@ __global__ void __launch_bounds__(kT) k_stats(StepArgs a) {
         const float c2[4] = {k2.x, k2.y, k2.z, k2.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          float m[3] = {m0[q], m1[q], m2[q]};
-          float v = vv[q];
+          const float m[3] = {m0[q], m1[q], m2[q]};
           const float c[3] = {c0[q], c1[q], c2[q]};
-          float f[kStats];
-          lopt_features(pp[q], gg[q], m, v, rt, c, f);
-#pragma unroll
-          for (int x = 0; x < kStats; ++x) acc[x] = ffma(f[x], f[x], acc[x]);
+          lopt_feature_squares(pp[q], gg[q], m, vv[q], r, c, inv_rho, acc);
         }
       }
     }

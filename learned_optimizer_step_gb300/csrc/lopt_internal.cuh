@@ -98,8 +98,8 @@ struct StepArgs {
 };
 
 // ---- exact, contraction-free fp32 helpers ----------------------------------
-// The statistics kernel and the apply kernel must compute bit-identical
-// features, so every operation is spelled out with a rounding intrinsic.
+// Every operation is spelled out with a rounding intrinsic, so that the
+// compiler contracts nothing and results do not depend on its choices.
 __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
 __device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
 __device__ __forceinline__ float ffma(float a, float b, float c) { return __fmaf_rn(a, b, c); }
@@ -169,6 +169,53 @@ __device__ __forceinline__ void lopt_features(float p, float g, float m[3], floa
   for (int a = 0; a < 3; ++a)
 #pragma unroll
     for (int b = 0; b < 3; ++b) f[19 + 3 * a + b] = fmul(m[a], rvh[b]);
+}
+
+// 1 / a: the PTX rcp.approx instruction (about 1 ulp).  Arguments here are
+// at least kEps = 1e-30, a normal number, so flushing never applies.
+__device__ __forceinline__ float frcp(float a) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+  return r;
+}
+
+// The statistics pass needs only the squares of the 28 features, and most of
+// them have a cheaper closed form than squaring the feature:
+//   (m rsqrt(v+eps))^2 = m^2 / (v+eps),   sqrt(v)^2 ~ v^2 / (v+eps),
+//   sqrt(r)^2 = r,   sqrt(c)^2 = c,   (m_a rsqrt(vhat_b+eps))^2 = m_a^2 / (vhat_b+eps).
+// This adds, for one element, the squares of its features (order as in
+// lopt_features) to acc, after the same accumulator update.
+__device__ __forceinline__ void lopt_feature_squares(float p, float g, const float m_old[3], float v_old,
+                                                     const float r[3], const float c[3],
+                                                     const float inv_rho[3], float acc[kStats]) {
+  float m[3], m2[3], ivh[3];
+  const float g2 = fmul(g, g);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    m[k] = ffma(beta(k), m_old[k], fmul(one_minus_beta(k), g));
+    m2[k] = fmul(m[k], m[k]);
+    ivh[k] = frcp(fadd(fmul(fmul(r[k], inv_rho[k]), c[k]), kEps));
+  }
+  const float v = ffma(kBeta2, v_old, fmul(kOneMinusBeta2, g2));
+  const float iv = frcp(fadd(v, kEps));
+  acc[0] = ffma(p, p, acc[0]);
+  acc[1] = fadd(acc[1], g2);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) acc[2 + k] = fadd(acc[2 + k], m2[k]);
+  acc[5] = ffma(fmul(v, v), iv, acc[5]);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) acc[6 + k] = ffma(m2[k], iv, acc[6 + k]);
+  acc[9] = ffma(g2, iv, acc[9]);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) acc[10 + k] = ffma(g2, ivh[k], acc[10 + k]);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) acc[13 + k] = fadd(acc[13 + k], r[k]);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) acc[16 + k] = fadd(acc[16 + k], c[k]);
+#pragma unroll
+  for (int a = 0; a < 3; ++a)
+#pragma unroll
+    for (int b = 0; b < 3; ++b) acc[19 + 3 * a + b] = ffma(m2[a], ivh[b], acc[19 + 3 * a + b]);
 }
 
 // Offsets inside one weight set (caller layout).
