@@ -48,7 +48,7 @@ __device__ __forceinline__ void accumulate_element(const TensorDesc& d, const fl
   lopt_feature_squares(__ldg(d.p + e), __ldg(d.g + e), m, __ldg(d.v + e), r, c, inv_rho, acc);
 }
 
-__global__ void __launch_bounds__(kT) k_stats(StepArgs a) {
+__global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per SM for loads in flight
   __shared__ float red[kWarps][kStats];
   __shared__ double scale[kStats];
   __shared__ int is_last;
