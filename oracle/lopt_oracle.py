@@ -39,6 +39,10 @@ R6  ReLU after both hidden layers, linear output, o0 = direction,
     o1 = magnitude.  Weights per set: W1[39][H], b1[H], W2[H][H], b2[H],
     W3[H][2], b3[2], row-major, concatenated in that order.
 R7  p <- p - lr * update.
+R11 Decoupled weight decay (section "学習率スケジュールと重み減衰の効果"
+    reports that schedules and weight decay change what a learned
+    optimiser reaches; it gives no formula): p <- p - lr * (update + wd * p)
+    with the parameter before the step, wd = 0 by default (then exactly R7).
 R8  t is the caller's 1-based step count.
 R10 See the tests for the error metric.
 
@@ -261,6 +265,11 @@ def update_from_output(o: np.ndarray) -> np.ndarray:
     return o[:, 0] * np.exp(o[:, 1] * OUTPUT_SCALE) * OUTPUT_SCALE
 
 
+def apply_update(p: np.ndarray, u: np.ndarray, lr: float, weight_decay: float = 0.0) -> np.ndarray:
+    """R7 / R11: p - lr * (u + weight_decay * p)."""
+    return p - lr * (u + weight_decay * p)
+
+
 # ---------------------------------------------------------------------------
 # One tensor, one step
 # ---------------------------------------------------------------------------
@@ -302,7 +311,7 @@ def refresh_accumulators(state: dict) -> None:
 
 
 def step_tensor(state: dict, t: float, lr: float, w: MLPWeights,
-                sample_idx: np.ndarray | None = None) -> dict:
+                sample_idx: np.ndarray | None = None, weight_decay: float = 0.0) -> dict:
     """One learned-optimizer step on one tensor, in place.
 
     Returns a dict of diagnostics: S (the 28 square sums), scales, and -- when
@@ -321,7 +330,7 @@ def step_tensor(state: dict, t: float, lr: float, w: MLPWeights,
         o = mlp(normalise(F, scales), w)
         u = update_from_output(o)
         out["sample_idx"] = sample_idx
-        out["sample_param"] = state["param"][sample_idx] - lr * u
+        out["sample_param"] = apply_update(state["param"][sample_idx], u, lr, weight_decay)
         out["sample_update"] = u
         return out
     new_p = np.empty_like(state["param"])
@@ -329,16 +338,16 @@ def step_tensor(state: dict, t: float, lr: float, w: MLPWeights,
         idx = np.arange(e0, min(n, e0 + CHUNK_ELEMENTS))
         F = _features_of(state, C, t, idx)
         o = mlp(normalise(F, scales), w)
-        new_p[idx] = state["param"][idx] - lr * update_from_output(o)
+        new_p[idx] = apply_update(state["param"][idx], update_from_output(o), lr, weight_decay)
     state["param"] = new_p
     return out
 
 
 def step(states: List[dict], t: float, lr: float, weight_sets: Sequence[np.ndarray],
-         hidden: int) -> List[dict]:
+         hidden: int, weight_decay: float = 0.0) -> List[dict]:
     """One step over a parameter list; each tensor uses its own weight set."""
     ws = [unpack_weights(wf, hidden) for wf in weight_sets]
-    return [step_tensor(st, t, lr, ws[st["weight_set"]]) for st in states]
+    return [step_tensor(st, t, lr, ws[st["weight_set"]], weight_decay=weight_decay) for st in states]
 
 
 def materialised_features(state: dict, t: float) -> np.ndarray:
@@ -354,6 +363,6 @@ __all__ = [
     "view_rows_cols", "weight_set_size", "MLPWeights", "unpack_weights",
     "factored_update", "factored_vhat", "accumulator_update", "time_features",
     "features", "feature_square_sums", "normalisation_scales", "normalise",
-    "mlp", "update_from_output", "new_state", "refresh_accumulators",
+    "mlp", "update_from_output", "apply_update", "new_state", "refresh_accumulators",
     "step_tensor", "step", "materialised_features",
 ]

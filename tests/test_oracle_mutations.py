@@ -21,6 +21,8 @@ PIN_TESTS = [
     pins.test_p4_second_relu_and_biases,
     pins.test_p6_gradient_scale_invariance,
     pins.test_p7_indexing_tags,
+    lambda: pins.test_p8_weight_decay_alone_is_geometric(0.3, 1e-2),
+    pins.test_p8_weight_decay_on_normalised_sgd,
 ]
 
 
@@ -120,6 +122,10 @@ MUTATIONS = {
                              lambda o: o[:, 0] * np.exp(o[:, 1]) * 1e-3),
     "time features off by one step": ("time_features",
                                       lambda t: np.tanh((float(t) + 1) / np.asarray(L.TIME_SCALES))),
+    "weight decay sign flipped": ("apply_update", lambda p, u, lr, wd=0.0: p - lr * (u - wd * p)),
+    "weight decay after the update": ("apply_update",
+                                      lambda p, u, lr, wd=0.0: (p - lr * u) * (1.0 - lr * wd)),
+    "weight decay not scaled by lr": ("apply_update", lambda p, u, lr, wd=0.0: p - lr * u - wd * p),
 }
 
 

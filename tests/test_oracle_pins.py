@@ -368,3 +368,52 @@ def test_view_rules():
     assert O.view_rows_cols((7,)) == (1, 7)
     assert O.view_rows_cols((2, 3, 4)) == (6, 4)
     assert O.weight_set_size(32) == 39 * 32 + 32 + 32 * 32 + 32 + 64 + 2
+
+
+# ---------------------------------------------------------------------------
+# P8: decoupled weight decay (reading R11)
+# ---------------------------------------------------------------------------
+def _zero_output_weights(H):
+    """Any W1, W2; zero output layer, so the learned update is exactly 0."""
+    rng = np.random.default_rng(11)
+    n = O.weight_set_size(H)
+    w = rng.normal(size=n) * 0.3
+    w[n - 2 * H - 2:] = 0.0      # W3[H][2] and b3[2] are the last 2H + 2 floats
+    return w
+
+
+@pytest.mark.parametrize("lr,wd", [(1.0, 0.1), (0.3, 1e-2), (2.0, 0.0)])
+def test_p8_weight_decay_alone_is_geometric(lr, wd):
+    """With the learned update identically zero, one step multiplies every
+    parameter by exactly (1 - lr * wd)."""
+    rng = np.random.default_rng(12)
+    R, C = 4, 7
+    p = rng.normal(size=R * C)
+    st = O.new_state((R, C), p, rng.normal(size=R * C) * 1e-3)
+    O.step_tensor(st, 3, lr, O.unpack_weights(_zero_output_weights(8), 8), weight_decay=wd)
+    np.testing.assert_allclose(st["param"], p * (1.0 - lr * wd), rtol=1e-15, atol=0)
+
+
+def test_p8_weight_decay_on_normalised_sgd():
+    """Identity routing plus decay: p - lr * (1e-3 e^(1e-3 c) g_hat + wd p),
+    decay taken on the parameter before the step."""
+    rng = np.random.default_rng(13)
+    R, C, lr, wd, c_mag = 3, 5, 0.7, 0.05, 40.0
+    p = rng.normal(size=R * C) * 0.02
+    g = rng.normal(size=R * C) * 2e-4
+    st = O.new_state((R, C), p, g)
+    O.step_tensor(st, 1, lr, O.unpack_weights(routing_weights(4, 1, c_mag), 4), weight_decay=wd)
+    ghat = g / np.sqrt(np.mean(g * g) + 1e-30)
+    expect = p - lr * (1e-3 * math.exp(1e-3 * c_mag) * ghat + wd * p)
+    np.testing.assert_allclose(st["param"], expect, rtol=1e-13, atol=1e-18)
+
+
+def test_p8_zero_decay_is_the_plain_step():
+    rng = np.random.default_rng(14)
+    w = O.unpack_weights(rng.normal(size=O.weight_set_size(8)) * 0.2, 8)
+    p = rng.normal(size=12)
+    g = rng.normal(size=12) * 1e-3
+    a, b = O.new_state((3, 4), p, g), O.new_state((3, 4), p, g)
+    O.step_tensor(a, 2, 0.5, w)
+    O.step_tensor(b, 2, 0.5, w, weight_decay=0.0)
+    assert np.array_equal(a["param"], b["param"])
