@@ -122,18 +122,31 @@ int lopt_create(const float* mlp_weights, int d_feat, int hidden, int n_sets,
 
 /*
  * Choose how the MLP is evaluated by later lopt_step() calls:
- * LOPT_MLP_FP32 (exact FP32 arithmetic) or LOPT_MLP_TC (tensor cores: TF32
- * first layer, FP16 second and output layers, FP32 accumulation; about 1e-3
- * relative error on the update).  LOPT_E_UNSUPPORTED if the path cannot run
- * this handle's hidden width.
+ * LOPT_MLP_FP32 (exact FP32 arithmetic) or LOPT_MLP_TC (tensor cores: FP16
+ * operands for the first two layers with FP32 accumulation, output layer in
+ * FP32; about 1e-3 relative error on the update).  LOPT_E_UNSUPPORTED if the
+ * path cannot run this handle's hidden width.
  */
 int lopt_set_mlp_path(lopt_handle h, int path);
+
+/*
+ * Decoupled weight decay for later lopt_step() calls: every element becomes
+ *   param <- param - lr * (update + weight_decay * param)
+ * with the parameter before the step (0 by default: param -= lr * update).
+ * The pages on PyLO report that learning-rate schedules and weight decay
+ * change what a learned optimiser reaches (section "学習率スケジュールと重み
+ * 減衰の効果"); the schedule is the caller's per-step lr.  Applied in the
+ * apply pass at no extra memory traffic.  LOPT_E_ARG if weight_decay is
+ * negative or not finite.
+ */
+int lopt_set_weight_decay(lopt_handle h, float weight_decay);
 
 /*
  * One learned-optimizer step over n_tensors tensors (HOST array of
  * descriptors; it is read during the call only).
  *   t       1-based step count (drives the 11 time features tanh(t / x_s)).
- *   lr      multiplies the update (param -= lr * update).
+ *   lr      multiplies the update (param -= lr * update, plus the decay set
+ *           by lopt_set_weight_decay()).
  *   stream  cudaStream_t to enqueue on (NULL = legacy default stream).
  * The whole list is processed by three kernel launches (row/column moments,
  * feature statistics, normalise + MLP + apply).  Asynchronous: returns once

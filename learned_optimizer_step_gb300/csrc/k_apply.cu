@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kT) k_apply_fp32(StepArgs a) {
 
   const int64_t e0 = (int64_t)u.local * kApplyChunk;
   const int64_t e1 = min(d.N, e0 + (int64_t)kApplyChunk);
-  const float lr = a.lr;
+  const float lr = a.lr, wd = a.wd;
 
   for (int64_t base = e0 + (int64_t)tid * E; base < e1; base += (int64_t)kT * E) {
     float f[E][kStats];
@@ -129,7 +129,7 @@ __global__ void __launch_bounds__(kT) k_apply_fp32(StepArgs a) {
     for (int e = 0; e < E; ++e) {
       if (!ok[e]) continue;
       const int64_t x = base + e;
-      d.p[x] = p[e] - lr * upd[e];
+      d.p[x] = p[e] - lr * (upd[e] + wd * p[e]);
 #pragma unroll
       for (int k = 0; k < 3; ++k) d.m[k][x] = m[e][k];
       d.v[x] = v[e];

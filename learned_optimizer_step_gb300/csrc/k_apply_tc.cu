@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
       const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
       const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
-      const float lr = a.lr;
+      const float lr = a.lr, wd = a.wd;
       StageIter si;
       si.init(a.units, a.desc, u0, u1);
       bool ok = true;
@@ -576,10 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           const float upd = o0 * ex * kOutScale;
           const int x = j * kTile + t;
           if (stg) {   // past the end: an unused stage word
-            pst[x] = pst[x] - lr * upd;
+            pst[x] = pst[x] - lr * (upd + wd * pst[x]);
           } else if (x < si.n) {
             float* pp = a.desc[rc.tensor].p + (rc.e0 + x);
-            *pp = *pp - lr * upd;
+            *pp = *pp - lr * (upd + wd * *pp);
           }
         }
         if (!ok) break;

@@ -10,6 +10,7 @@
 // "メモリ階層の活用") counts 30-114 launches per step for a whole model with
 // its two fused kernels per tensor; here the whole list takes three.
 #include <algorithm>
+#include <cmath>
 #include <cstddef>
 #include <cstdio>
 #include <cstdlib>
@@ -45,6 +46,7 @@ struct lopt_ctx {
   int hp = 0;            // padded width used by the kernels
   int n_sets = 0;
   int path = LOPT_MLP_FP32;
+  float weight_decay = 0.f;
   float* d_weights = nullptr;  // [n_sets][w_set_size(hp)], zero-padded
   void* d_tcw = nullptr;       // packed FP16 layer-2/3 operands (tensor-core path)
   // workspace
@@ -330,6 +332,12 @@ int lopt_set_mlp_path(lopt_handle h, int path) {
   return LOPT_E_ARG;
 }
 
+int lopt_set_weight_decay(lopt_handle h, float weight_decay) {
+  if (!h || !(weight_decay >= 0.f) || !std::isfinite(weight_decay)) return LOPT_E_ARG;
+  h->weight_decay = weight_decay;
+  return LOPT_OK;
+}
+
 int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t t, float lr,
               void* stream_ptr) {
   if (!h || n_tensors < 0 || (n_tensors > 0 && !tensors)) return LOPT_E_ARG;
@@ -382,6 +390,7 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   a.tc_weights = h->d_tcw;
   a.t = (double)t;
   a.lr = lr;
+  a.wd = h->weight_decay;
   a.status = h->d_status;
 
   cudaEvent_t* ev = nullptr;

@@ -94,6 +94,7 @@ struct StepArgs {
   const void*       tc_weights;  // per-set packed FP16 B operands (tensor-core path)
   double            t;           // step count
   float             lr;
+  float             wd;          // decoupled weight decay: p -= lr * (update + wd * p)
   int32_t*          status;      // device-side error flags
 };
 

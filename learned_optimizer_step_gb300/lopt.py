@@ -31,7 +31,7 @@ ERRORS = {
     -9: "LOPT_E_TOO_LARGE",
 }
 
-EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_step",
+EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_set_weight_decay", "lopt_step",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
             "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_version")
 
@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_create.restype = i32
     lib.lopt_set_mlp_path.argtypes = [vp, i32]
     lib.lopt_set_mlp_path.restype = i32
+    lib.lopt_set_weight_decay.argtypes = [vp, ctypes.c_float]
+    lib.lopt_set_weight_decay.restype = i32
     lib.lopt_step.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, i64, ctypes.c_float, vp]
     lib.lopt_step.restype = i32
     lib.lopt_check.argtypes = [vp]
@@ -181,6 +183,10 @@ class LearnedOptimizer:
     def set_mlp_path(self, path: str) -> None:
         _check("lopt_set_mlp_path", load_library().lopt_set_mlp_path(self._h, _PATHS[path]))
         self.mlp_path = path
+
+    def set_weight_decay(self, weight_decay: float) -> None:
+        """Decoupled weight decay of later steps: p -= lr * (update + wd * p)."""
+        _check("lopt_set_weight_decay", load_library().lopt_set_weight_decay(self._h, float(weight_decay)))
 
     def prepare(self, tensors: Sequence) -> PreparedList:
         ts = [t if isinstance(t, TensorState) else TensorState.from_dict(t) for t in tensors]

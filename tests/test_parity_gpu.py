@@ -266,3 +266,49 @@ def test_gpt2_heavy_tails_late_step_sampled(path, tol):
         assert rel_err(got, want) <= elem_tol(tol), (st["name"], rel_err(got, want))
         assert rel_err(eng.feature_stats(idx), out["S"], floor=1e-300) <= 2e-5, st["name"]
     assert num / den <= tol, num / den
+
+
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_decoupled_weight_decay(path, tol):
+    """p - lr * (update + wd * p) against the oracle with the same decay; the
+    tensor list mixes staged and misaligned tensors."""
+    torch = need_gpu()
+    eng, w = engine(path=path)
+    eng.set_weight_decay(0.05)
+    states = make_states([("a", (96, 130)), ("b", (257,)), ("c", (40, 64))], recipe="vit", seed=3)
+    ref = [to_oracle(s) for s in states]
+    eng.step(states, 4, 0.7)
+    eng.check()
+    torch.cuda.synchronize()
+    ws = O.unpack_weights(w[0], 32)
+    num = den = 0.0
+    for st, r in zip(states, ref):
+        O.step_tensor(r, 4, 0.7, ws, weight_decay=0.05)
+        got = cpu(st["param"])
+        num = max(num, float(np.max(np.abs(got - r["param"]))))
+        den = max(den, float(np.max(np.abs(r["param"]))))
+        assert rel_err(got, r["param"]) <= elem_tol(tol)
+    assert num / den <= tol
+
+
+@pytest.mark.parametrize("path", ["fp32", "tc"])
+def test_zero_weight_decay_is_bitwise_the_plain_step(path):
+    torch = need_gpu()
+    a, _ = engine(path=path)
+    b, _ = engine(path=path)
+    b.set_weight_decay(0.0)
+    sa = make_states([("a", (64, 200))], recipe="vit", seed=4)
+    sb = make_states([("a", (64, 200))], recipe="vit", seed=4)
+    a.step(sa, 1, 1.0)
+    b.step(sb, 1, 1.0)
+    torch.cuda.synchronize()
+    assert torch.equal(sa[0]["param"], sb[0]["param"])
+
+
+def test_weight_decay_rejects_bad_values():
+    need_gpu()
+    from learned_optimizer_step_gb300 import LoptError
+    eng, _ = engine()
+    for bad in (-0.1, float("nan"), float("inf")):
+        with pytest.raises(LoptError):
+            eng.set_weight_decay(bad)
