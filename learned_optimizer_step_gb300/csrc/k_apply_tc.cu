@@ -369,7 +369,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
         int s = si.k0 % S;                          // slot of the stage's first tile
         uint32_t sph = (uint32_t)((si.k0 / S) & 1);  // its round parity
         for (int j = 0; j < ntl; ++j) {
-          if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) { ok = false; break; }
           const int x = j * kTile + t;                 // element offset in the stage
           const int xi = min(x, si.n - 1);             // past the end: index math of the last element
           float p, g, m[3], v;
@@ -430,6 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           }
           av[14] = 0x00003C00u;   // 1.0h, 0
           av[15] = 0u;
+          // the tile's slot is needed only now: loads and arithmetic above
+          // overlap the wait for it
+          if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) { ok = false; break; }
           tmem_st16(t_lane + s * G::SlotCols + NP, av);
           tmem_wait_st();
           tc_fence_before();
