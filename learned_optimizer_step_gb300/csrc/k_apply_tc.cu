@@ -58,19 +58,28 @@ namespace lopt {
 namespace {
 
 constexpr int kTile = 128;                // elements per tile (= TMEM lanes)
-constexpr int kThreads = 19 * 32;         // 8 epilogue + 8 feature + producer + 2 MMA warps
+constexpr int kEpiGroups = 2;             // epilogue warpgroups (stages in rotation)
+constexpr int kFeatGroups = 2;            // feature warpgroups (stages in rotation)
+// Measured on the ViT-B/16 list: three epilogue groups (80 registers per
+// thread) are slower than two; three feature groups deadlock in the slot
+// rotation, so the pipeline is built for two of each.
+static_assert(kFeatGroups == 2 && kEpiGroups >= 2, "pipeline depth analysis assumes two feature groups");
+constexpr int kFeatWarp0 = 4 * kEpiGroups;                    // first feature warp
+constexpr int kProducerWarp = kFeatWarp0 + 4 * kFeatGroups;   // then the producer
+constexpr int kMma1Warp = kProducerWarp + 1, kMma2Warp = kProducerWarp + 2;
+constexpr int kThreads = (kMma2Warp + 1) * 32;
 constexpr int kStageTiles = 8;            // tiles per stage (4 KB per array)
 constexpr int kStageElems = kStageTiles * kTile;
 constexpr int kArrays = 6;                // p, g, m0, m1, m2, v
 constexpr int kRingStages = 6;            // stages held in shared memory
 constexpr int kStageBytes = kArrays * kStageElems * 4;
 constexpr int kStageUsers = 2 * kTile;    // the feature and the epilogue group that own a stage
-// Commit barriers per layer, one per tile in rotation.  A thread waiting for
-// tile j has not yet freed the slot of its tile, so no MMA thread can commit
-// tile j + S; with at least S barriers a waiter never sees its barrier
-// lapped.
-constexpr int kDone = 16;
-constexpr int kProducerWarp = 16, kMma1Warp = 17, kMma2Warp = 18;
+// Commit barriers per layer, one per tile in rotation; a waiter must never
+// see its barrier lapped.  While an epilogue thread waits for tile j, the
+// slots of j and of the later tiles of its stage stay taken, so the MMA
+// threads can get no further ahead than the stages the other epilogue groups
+// own plus one slot round: fewer than kEpiGroups * kStageTiles + S tiles.
+constexpr int kDone = 64;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 // Where stage array q (p, g, m0, m1, m2, v) of a tensor lives.
@@ -126,7 +135,7 @@ struct Geom {
   static_assert(Smem <= 232448, "shared memory of one CTA");
   // an epilogue group finishes layer 1 of all tiles of a stage before the
   // rest of any: the stage's last tile must not wait for a slot of its own
-  static_assert(S * SlotCols <= 512 && S >= kStageTiles && kDone >= S,
+  static_assert(S * SlotCols <= 512 && S >= kStageTiles && kDone >= kEpiGroups * kStageTiles + S,
                 "tensor memory columns / pipeline depth");
   static_assert(oRec % 16 == 0 && sizeof(StageRec) % 16 == 0, "16-byte aligned stage records");
 };
@@ -349,18 +358,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           mbar_drain(ring_full + x % R, (uint32_t)((x / R) & 1), kWaitNs / 10);
       }
       bulk_wait_all();   // every write-back complete before the session ends
-    } else if (warp >= 8 && warp < 16) {
+    } else if (warp >= kFeatWarp0 && warp < kProducerWarp) {
       // --------------------------- feature warpgroups ------------------------
       // Group grp owns the stages n with n % 2 == grp and builds the A
       // operand of layer 1 for each of their tiles in order.
-      const int grp = (warp - 8) >> 2;
-      const int t = tid - 256 - 128 * grp;
+      const int grp = (warp - kFeatWarp0) >> 2;
+      const int t = tid - 32 * kFeatWarp0 - 128 * grp;
       const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
       StageIter si;
       si.init(a.units, a.desc, u0, u1);
       bool ok = true;
       for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
-        if ((ns & 1) != grp) continue;
+        if (ns % kFeatGroups != grp) continue;
         if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
         const StageRec& rc = rec[si.st];
         const bool stg = rc.bytes != 0;
@@ -469,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
         // nothing of ours may still be running when the session ends
         if (k > 0) mbar_drain(fin + ((k - 1) & (kDone - 1)), (uint32_t)(((k - 1) / kDone) & 1), kWaitNs / 10);
       }
-    } else if (warp < 8) {
+    } else if (warp < kFeatWarp0) {
       // ------------------------------ epilogue -------------------------------
       // Group h owns the stages n with n % 2 == h.  For a stage it first
       // finishes layer 1 of every tile (ReLU, FP16 A operand of layer 2, b2
@@ -486,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       si.init(a.units, a.desc, u0, u1);
       bool ok = true;
       for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
-        if ((ns & 1) != h) continue;
+        if (ns % kEpiGroups != h) continue;
         // the stage's record (written by the producer before it was loaded)
         if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
         const int ntl = (si.n + kTile - 1) / kTile;
