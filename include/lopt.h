@@ -161,6 +161,44 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
               int64_t t, float lr, void* stream);
 
 /*
+ * ---- Row-sharded step (data parallel over ranks) --------------------------
+ * The step of the PyLO pages' distributed optimiser (section "分散最適化
+ * ステップ": each rank owns a slice of the optimiser state, as after a
+ * reduce-scatter of the gradients).  Every rank owns whole rows of each
+ * tensor; the only quantities that need all rows are the column means of
+ * g^2, the mean of the row accumulators (rho) and the 28 feature square
+ * sums, so a step is three calls with two sums over the ranks in between:
+ *
+ *   lopt_shard_begin   row moments of the local rows; writes this rank's
+ *                      column sums of g^2 and row-accumulator sums to x1
+ *   (caller: x1 <- sum of x1 over the ranks, e.g. an all-reduce)
+ *   lopt_shard_middle  column accumulators and rho from x1; writes this
+ *                      rank's feature square sums to x2
+ *   (caller: x2 <- sum of x2 over the ranks)
+ *   lopt_shard_end     normalisation from x2, MLP, update of the local rows
+ *
+ * Every rank passes the same list: same tensors, order, cols and weight
+ * sets; tensors[i].rows is the number of rows this rank owns (0 allowed:
+ * then only col[k] is read, the other pointers may be NULL) and
+ * global_rows[i] the rows of the whole tensor.  The column accumulators are
+ * replicated: every rank passes its own copy and all copies stay equal.
+ * The ranks' rows of a tensor must add up to global_rows[i]; rows are in
+ * any order.  With one rank owning everything the results equal
+ * lopt_step() up to the rounding of the sums.
+ *
+ * x1, x2: caller-owned DEVICE buffers of n_x1, n_x2 doubles
+ * (lopt_shard_sizes), read and written by the kernels of this step only;
+ * lopt_shard_begin zeroes them.  All three calls are asynchronous on their
+ * stream and ordered with each other; no other step of the handle may run
+ * between them (LOPT_E_ARG).  Errors as lopt_step().
+ */
+int lopt_shard_sizes(const lopt_tensor* tensors, int n_tensors, int64_t* n_x1, int64_t* n_x2);
+int lopt_shard_begin(lopt_handle h, const lopt_tensor* tensors, const int64_t* global_rows,
+                     int n_tensors, int64_t t, float lr, double* x1, double* x2, void* stream);
+int lopt_shard_middle(lopt_handle h, void* stream);
+int lopt_shard_end(lopt_handle h, void* stream);
+
+/*
  * Wait for the handle's last step and report device-side status:
  * LOPT_OK, LOPT_E_TIMEOUT (a bounded wait inside a kernel gave up; that
  * step's results are invalid) or LOPT_E_CUDA.  Clears the status.

@@ -229,7 +229,21 @@ __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
   const float* cp = a.colpart + d.colpart_off;
   const double invR = 1.0 / (double)d.R;
   const int S = d.n_strips;
-  if (d.vec4 && (d.C % 4 == 0)) {
+  double* const xout = a.xch1 ? a.xch1 + d.x1_off : nullptr;   // row-sharded: sums go out
+  if (xout) {
+    for (int64_t j = tid; j < d.C; j += kT) {
+      double s = 0.0;
+#pragma unroll 8
+      for (int st = 0; st < S; ++st) s += (double)__ldcg(cp + (int64_t)st * d.C + j);
+      xout[j] = s;
+    }
+    if (tid < 3) {
+      double s = 0.0;
+      const double* rp = a.rowpart + d.rowpart_off;
+      for (int st = 0; st < d.n_strips; ++st) s += __ldcg(rp + 3 * st + tid);
+      xout[d.C + tid] = s;
+    }
+  } else if (d.vec4 && (d.C % 4 == 0)) {
     for (int64_t j = 4 * (int64_t)tid; j < d.C; j += 4 * (int64_t)kT) {
       double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
 #pragma unroll 8
@@ -262,7 +276,7 @@ __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
       }
     }
   }
-  if (tid < 3) {
+  if (!xout && tid < 3) {
     double s = 0.0;
     const double* rp = a.rowpart + d.rowpart_off;
     for (int st = 0; st < d.n_strips; ++st) s += __ldcg(rp + 3 * st + tid);
@@ -272,11 +286,37 @@ __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
   if (tid == 0) a.counters[u.tensor] = 0;
 }
 
+// Row-sharded steps: the column means and rho of every tensor from the sums
+// of all ranks (xch1, already added up), with the tensor's global row count.
+__global__ void __launch_bounds__(kT) k_rowcol_finish(StepArgs a) {
+  const TensorDesc d = a.desc[blockIdx.x];
+  const double* x = a.xch1 + d.x1_off;
+  const double invR = 1.0 / (double)d.Rg;
+  for (int64_t j = threadIdx.x; j < d.C; j += kT) {
+    const float H = (float)(x[j] * invR);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      float* c = d.c[k] + j;
+      *c = ffma(beta(k), *c, fmul(one_minus_beta(k), H));
+    }
+  }
+  if (threadIdx.x < 3) {
+    const double rho = x[d.C + threadIdx.x] * invR;
+    a.aux[blockIdx.x].inv_rho[threadIdx.x] = rho > 0.0 ? (float)(1.0 / rho) : 0.f;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rowcol(const StepArgs& a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
   k_rowcol<<<a.n_units, kT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rowcol_finish(const StepArgs& a, int n_tensors, cudaStream_t s) {
+  if (n_tensors == 0) return cudaSuccess;
+  k_rowcol_finish<<<n_tensors, kT, 0, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -48,6 +48,33 @@ __device__ __forceinline__ void accumulate_element(const TensorDesc& d, const fl
   lopt_feature_squares(__ldg(d.p + e), __ldg(d.g + e), m, __ldg(d.v + e), r, c, inv_rho, acc);
 }
 
+// Normalisation and time features folded into the first layer of tensor T
+// (run by a whole block): x_hat . W1 = sum_d f_d (s_d W1[d]) + sum_s tau_s W1[28 + s].
+__device__ void fold_first_layer(const StepArgs& a, int T, const TensorDesc& d, const double* scale) {
+  const int tid = threadIdx.x;
+  const int H = a.hidden;
+  const float* W = a.weights + (int64_t)d.wset * a.set_size;
+  const float* W1 = W + w_off_W1(H);
+  const float* b1 = W + w_off_b1(H);
+  float* out = a.w1fold + (int64_t)T * a.w1fold_stride;
+  if (a.path == LOPT_MLP_FP32) {
+    // layout: W1'[28][H] then b1'[H]
+    for (int x = tid; x < kStats * H; x += kT) {
+      const int dd = x / H;
+      out[x] = (float)(scale[dd] * (double)W1[x]);
+    }
+    for (int h = tid; h < H; h += kT) {
+      double b = (double)b1[h];
+      for (int s = 0; s < kTimeFeat; ++s) {
+        b += tanh(a.t / time_scale(s)) * (double)W1[(kStats + s) * H + h];
+      }
+      out[kStats * H + h] = (float)b;
+    }
+  } else {
+    fold_w1_tc(H, W1, b1, a.t, out);
+  }
+}
+
 __global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per SM for loads in flight
   __shared__ float red[kWarps][kStats];
   __shared__ double scale[kStats];
@@ -135,35 +162,34 @@ __global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per
     const float* part = a.k1part + d.k1_part_off;
     double s = 0.0;
     for (int x = 0; x < d.k1_units; ++x) s += (double)__ldcg(part + (int64_t)x * kStats + tid);
-    a.aux[u.tensor].S[tid] = s;
-    scale[tid] = 1.0 / sqrt(s / (double)d.N + 1e-30);
-    a.aux[u.tensor].scale[tid] = (float)scale[tid];
-  }
-  __syncthreads();
-
-  // Fold normalisation and time features into the first layer.
-  const int H = a.hidden;
-  const float* W = a.weights + (int64_t)d.wset * a.set_size;
-  const float* W1 = W + w_off_W1(H);
-  const float* b1 = W + w_off_b1(H);
-  float* out = a.w1fold + (int64_t)u.tensor * a.w1fold_stride;
-  if (a.path == LOPT_MLP_FP32) {
-    // layout: W1'[28][H] then b1'[H]
-    for (int x = tid; x < kStats * H; x += kT) {
-      const int dd = x / H;
-      out[x] = (float)(scale[dd] * (double)W1[x]);
+    if (a.xch2) {   // row-sharded: this rank's sums go out for the exchange
+      a.xch2[(int64_t)u.tensor * kStats + tid] = s;
+    } else {
+      a.aux[u.tensor].S[tid] = s;
+      scale[tid] = 1.0 / sqrt(s / (double)d.N + 1e-30);
+      a.aux[u.tensor].scale[tid] = (float)scale[tid];
     }
-    for (int h = tid; h < H; h += kT) {
-      double b = (double)b1[h];
-      for (int s = 0; s < kTimeFeat; ++s) {
-        b += tanh(a.t / time_scale(s)) * (double)W1[(kStats + s) * H + h];
-      }
-      out[kStats * H + h] = (float)b;
-    }
-  } else {
-    fold_w1_tc(H, W1, b1, a.t, out);
   }
   if (tid == 0) a.counters[u.tensor] = 0;
+  if (a.xch2) return;
+  __syncthreads();
+  fold_first_layer(a, u.tensor, d, scale);
+}
+
+// Row-sharded steps: S_d of every tensor from the sums of all ranks (xch2,
+// already added up) over the tensor's global element count, then the fold.
+__global__ void __launch_bounds__(kT) k_stats_finish(StepArgs a) {
+  __shared__ double scale[kStats];
+  const int T = blockIdx.x, tid = threadIdx.x;
+  const TensorDesc d = a.desc[T];
+  if (tid < kStats) {
+    const double s = a.xch2[(int64_t)T * kStats + tid];
+    a.aux[T].S[tid] = s;
+    scale[tid] = 1.0 / sqrt(s / ((double)d.Rg * (double)d.C) + 1e-30);
+    a.aux[T].scale[tid] = (float)scale[tid];
+  }
+  __syncthreads();
+  fold_first_layer(a, T, d, scale);
 }
 
 }  // namespace
@@ -171,6 +197,12 @@ __global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per
 cudaError_t launch_stats(const StepArgs& a, cudaStream_t s) {
   if (a.n_units == 0) return cudaSuccess;
   k_stats<<<a.n_units, kT, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats_finish(const StepArgs& a, int n_tensors, cudaStream_t s) {
+  if (n_tensors == 0) return cudaSuccess;
+  k_stats_finish<<<n_tensors, kT, 0, s>>>(a);
   return cudaGetLastError();
 }
 

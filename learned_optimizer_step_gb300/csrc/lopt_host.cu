@@ -67,7 +67,13 @@ struct lopt_ctx {
   int n_tensors = 0;
   // cached schedule key
   std::vector<lopt_tensor> last_list;
+  std::vector<int64_t> last_grows;   // global rows of a row-sharded schedule (empty: plain)
   int last_path = -1;
+  // row-sharded step in progress: 0 idle, 1 after begin, 2 after middle
+  int shard_phase = 0;
+  StepArgs shard_args;
+  double* x1 = nullptr;
+  double* x2 = nullptr;
   // ordering across calls
   cudaEvent_t done = nullptr;
   bool has_done = false;
@@ -96,13 +102,27 @@ struct Interval {
   uintptr_t lo, hi;
 };
 
-int validate(const lopt_ctx* h, const lopt_tensor* ts, int n) {
+// global_rows: null for a plain step; for a row-sharded step the rows of
+// each whole tensor, and a rank may hold none of a tensor's rows.
+int validate(const lopt_ctx* h, const lopt_tensor* ts, int n, const int64_t* global_rows = nullptr) {
   std::vector<Interval> iv;
   iv.reserve((size_t)n * 12);
   for (int i = 0; i < n; ++i) {
     const lopt_tensor& t = ts[i];
     if (t.reserved != 0) return LOPT_E_ARG;
     if (t.weight_set < 0 || t.weight_set >= h->n_sets) return LOPT_E_ARG;
+    if (global_rows) {
+      if (t.rows < 0 || t.cols < 1 || global_rows[i] < 1 || global_rows[i] < t.rows) return LOPT_E_SHAPE;
+      if (global_rows[i] > (int64_t)1 << 40) return LOPT_E_SHAPE;
+      if (t.rows == 0) {   // only the column accumulators on this rank
+        for (int k = 0; k < 3; ++k) {
+          if (!t.col[k]) return LOPT_E_ARG;
+          if ((uintptr_t)t.col[k] % 4) return LOPT_E_ALIGN;
+          iv.push_back({(uintptr_t)t.col[k], (uintptr_t)t.col[k] + (uintptr_t)t.cols * 4});
+        }
+        continue;
+      }
+    }
     if (t.rows < 1 || t.cols < 1) return LOPT_E_SHAPE;
     if (t.rows > (int64_t)1 << 31 || t.cols > (int64_t)1 << 31) return LOPT_E_SHAPE;
     const int64_t N = t.rows * t.cols;
@@ -128,10 +148,11 @@ int validate(const lopt_ctx* h, const lopt_tensor* ts, int n) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t stream) {
+int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t stream,
+                   const int64_t* global_rows = nullptr) {
   std::vector<TensorDesc> desc(n);
   std::vector<Unit> units[3];
-  int64_t colpart = 0, rowpart = 0, k1part = 0;
+  int64_t colpart = 0, rowpart = 0, k1part = 0, x1 = 0;
   for (int i = 0; i < n; ++i) {
     const lopt_tensor& t = ts[i];
     TensorDesc& d = desc[i];
@@ -151,7 +172,10 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
     bool v4 = aligned16(t.param) && aligned16(t.grad) && aligned16(t.rms);
     for (int k = 0; k < 3; ++k) v4 = v4 && aligned16(t.mom[k]) && aligned16(t.col[k]);
     d.vec4 = v4 ? 1 : 0;
-    d.strip_rows = strip_rows_for(d.R, d.C);
+    d.Rg = global_rows ? global_rows[i] : d.R;
+    d.x1_off = x1;
+    x1 += d.C + 3;
+    d.strip_rows = d.R > 0 ? strip_rows_for(d.R, d.C) : 1;
     d.n_strips = (int)((d.R + d.strip_rows - 1) / d.strip_rows);
     d.k1_units = (int)((d.N + kStatsChunk - 1) / kStatsChunk);
     d.k2_units = (int)((d.N + kApplyChunk - 1) / kApplyChunk);
@@ -234,7 +258,48 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
   for (int k = 0; k < 3; ++k) h->n_units[k] = (int)units[k].size();
   h->n_tensors = n;
   h->last_list.assign(ts, ts + n);
+  if (global_rows) h->last_grows.assign(global_rows, global_rows + n);
+  else h->last_grows.clear();
   h->last_path = h->path;
+  return LOPT_OK;
+}
+
+// Row-sharded exchange sizes: buffer 1 holds C + 3 doubles per tensor,
+// buffer 2 holds 28.
+void shard_counts(const lopt_tensor* ts, int n, int64_t* n1, int64_t* n2) {
+  int64_t a = 0;
+  for (int i = 0; i < n; ++i) a += ts[i].cols + 3;
+  *n1 = a;
+  *n2 = (int64_t)kStats * n;
+}
+
+}  // namespace
+
+namespace {
+
+// Device, ordering and the common launch arguments of one sharded phase.
+struct PhaseScope {
+  int prev = -1, want = 0;
+  ~PhaseScope() { if (prev >= 0 && prev != want) cudaSetDevice(prev); }
+};
+
+int enter_phase(lopt_ctx* h, cudaStream_t stream, PhaseScope& sc) {
+  cudaError_t e = cudaGetDevice(&sc.prev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  sc.want = h->device;
+  if (sc.prev != h->device && (e = cudaSetDevice(h->device)) != cudaSuccess) return cuda_fail(e);
+  if (h->has_done && (e = cudaStreamWaitEvent(stream, h->done, 0)) != cudaSuccess) return cuda_fail(e);
+  return LOPT_OK;
+}
+
+int leave_phase(lopt_ctx* h, cudaStream_t stream, cudaError_t e) {
+  if (e == cudaSuccess) e = cudaEventRecord(h->done, stream);
+  if (e != cudaSuccess) {
+    h->shard_phase = 0;
+    h->last_list.clear();
+    return cuda_fail(e);
+  }
+  h->has_done = true;
   return LOPT_OK;
 }
 
@@ -345,7 +410,9 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   if (n_tensors == 0) return LOPT_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
 
-  const bool same = h->last_path == h->path && (int)h->last_list.size() == n_tensors &&
+  if (h->shard_phase != 0) return LOPT_E_ARG;   // a row-sharded step is in progress
+  const bool same = h->last_path == h->path && h->last_grows.empty() &&
+                    (int)h->last_list.size() == n_tensors &&
                     std::memcmp(h->last_list.data(), tensors, sizeof(lopt_tensor) * n_tensors) == 0;
   if (!same) {
     int rc = validate(h, tensors, n_tensors);
@@ -438,6 +505,106 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   if (e != cudaSuccess) return cuda_fail(e);
   h->has_done = true;
   return LOPT_OK;
+}
+
+int lopt_shard_sizes(const lopt_tensor* tensors, int n_tensors, int64_t* n_x1, int64_t* n_x2) {
+  if (n_tensors < 0 || (n_tensors > 0 && !tensors) || !n_x1 || !n_x2) return LOPT_E_ARG;
+  shard_counts(tensors, n_tensors, n_x1, n_x2);
+  return LOPT_OK;
+}
+
+int lopt_shard_begin(lopt_handle h, const lopt_tensor* tensors, const int64_t* global_rows,
+                     int n_tensors, int64_t t, float lr, double* x1, double* x2, void* stream_ptr) {
+  if (!h || n_tensors < 1 || !tensors || !global_rows || !x1 || !x2 || t < 1) return LOPT_E_ARG;
+  if (h->shard_phase != 0) return LOPT_E_ARG;
+  if ((uintptr_t)x1 % 8 || (uintptr_t)x2 % 8) return LOPT_E_ALIGN;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  const bool same = h->last_path == h->path && (int)h->last_list.size() == n_tensors &&
+                    (int)h->last_grows.size() == n_tensors &&
+                    std::memcmp(h->last_list.data(), tensors, sizeof(lopt_tensor) * n_tensors) == 0 &&
+                    std::memcmp(h->last_grows.data(), global_rows, sizeof(int64_t) * n_tensors) == 0;
+  if (!same) {
+    const int rc = validate(h, tensors, n_tensors, global_rows);
+    if (rc != LOPT_OK) return rc;
+  }
+  PhaseScope sc;
+  int rc = enter_phase(h, stream, sc);
+  if (rc != LOPT_OK) return rc;
+  if (!same) {
+    rc = build_schedule(h, tensors, n_tensors, stream, global_rows);
+    if (rc != LOPT_OK) {
+      h->last_list.clear();
+      return rc;
+    }
+  }
+  int64_t n1 = 0, n2 = 0;
+  shard_counts(tensors, n_tensors, &n1, &n2);
+  StepArgs& a = h->shard_args;
+  std::memset(&a, 0, sizeof(a));
+  a.desc = h->d_desc;
+  a.hidden = h->hp;
+  a.aux = h->d_aux;
+  a.colpart = h->d_colpart;
+  a.rowpart = h->d_rowpart;
+  a.k1part = h->d_k1part;
+  a.weights = h->d_weights;
+  a.set_size = w_set_size(h->hp);
+  a.w1fold = h->d_w1fold;
+  a.w1fold_stride = h->w1fold_stride;
+  a.path = h->path;
+  a.tc_weights = h->d_tcw;
+  a.t = (double)t;
+  a.lr = lr;
+  a.wd = h->weight_decay;
+  a.status = h->d_status;
+  h->x1 = x1;
+  h->x2 = x2;
+  cudaError_t e = cudaMemsetAsync(x1, 0, sizeof(double) * n1, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(x2, 0, sizeof(double) * n2, stream);
+  StepArgs k0 = a;
+  k0.units = h->d_units[0];
+  k0.n_units = h->n_units[0];
+  k0.counters = h->d_counters;
+  k0.xch1 = x1;
+  if (e == cudaSuccess) e = launch_rowcol(k0, stream);
+  h->shard_phase = 1;
+  return leave_phase(h, stream, e);
+}
+
+int lopt_shard_middle(lopt_handle h, void* stream_ptr) {
+  if (!h || h->shard_phase != 1) return LOPT_E_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  PhaseScope sc;
+  const int rc = enter_phase(h, stream, sc);
+  if (rc != LOPT_OK) return rc;
+  StepArgs f = h->shard_args;
+  f.xch1 = h->x1;
+  cudaError_t e = launch_rowcol_finish(f, h->n_tensors, stream);
+  StepArgs k1 = h->shard_args;
+  k1.units = h->d_units[1];
+  k1.n_units = h->n_units[1];
+  k1.counters = h->d_counters + h->n_tensors;
+  k1.xch2 = h->x2;
+  if (e == cudaSuccess) e = launch_stats(k1, stream);
+  h->shard_phase = 2;
+  return leave_phase(h, stream, e);
+}
+
+int lopt_shard_end(lopt_handle h, void* stream_ptr) {
+  if (!h || h->shard_phase != 2) return LOPT_E_ARG;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+  PhaseScope sc;
+  const int rc = enter_phase(h, stream, sc);
+  if (rc != LOPT_OK) return rc;
+  StepArgs f = h->shard_args;
+  f.xch2 = h->x2;
+  cudaError_t e = launch_stats_finish(f, h->n_tensors, stream);
+  StepArgs k2 = h->shard_args;
+  k2.units = h->d_units[2];
+  k2.n_units = h->n_units[2];
+  if (e == cudaSuccess) e = (h->path == LOPT_MLP_TC) ? launch_apply_tc(k2, stream) : launch_apply_fp32(k2, stream);
+  h->shard_phase = 0;
+  return leave_phase(h, stream, e);
 }
 
 int lopt_check(lopt_handle h) {

@@ -59,6 +59,8 @@ struct TensorDesc {
   int64_t      colpart_off;   // K0 column partials: n_strips * C floats
   int32_t      rowpart_off;   // K0 row partials: n_strips * 3 doubles
   int32_t      k1_part_off;   // K1 partials: k1_units * kStats floats
+  int64_t      Rg;            // row-sharded steps: rows of the whole tensor over all ranks
+  int64_t      x1_off;        // row-sharded steps: offset of this tensor in exchange buffer 1
 };
 
 // A work unit: tensor index and the unit's index inside the tensor.
@@ -95,6 +97,12 @@ struct StepArgs {
   double            t;           // step count
   float             lr;
   float             wd;          // decoupled weight decay: p -= lr * (update + wd * p)
+  // Row-sharded steps only (null otherwise): this rank's sums that the ranks
+  // add up between the kernels.  xch1: per tensor, the C column sums of g^2
+  // then the 3 sums of the new row accumulators; xch2: per tensor, the 28
+  // feature square sums.
+  double*           xch1;
+  double*           xch2;
   int32_t*          status;      // device-side error flags
 };
 
@@ -235,6 +243,9 @@ enum : int32_t { kStatusTimeout = 1 };
 cudaError_t launch_rowcol(const StepArgs& a, cudaStream_t s);
 int  strip_rows_for(int64_t R, int64_t C);   // K0 rows per strip of an [R x C] tensor
 cudaError_t launch_stats(const StepArgs& a, cudaStream_t s);
+// Row-sharded steps: finish every tensor from the exchanged sums.
+cudaError_t launch_rowcol_finish(const StepArgs& a, int n_tensors, cudaStream_t s);
+cudaError_t launch_stats_finish(const StepArgs& a, int n_tensors, cudaStream_t s);
 cudaError_t launch_apply_fp32(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_apply_tc(const StepArgs& a, cudaStream_t s);
 bool apply_tc_supported(int hidden);

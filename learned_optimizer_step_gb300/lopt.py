@@ -32,6 +32,7 @@ ERRORS = {
 }
 
 EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_set_weight_decay", "lopt_step",
+            "lopt_shard_sizes", "lopt_shard_begin", "lopt_shard_middle", "lopt_shard_end",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
             "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_version")
 
@@ -76,6 +77,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_set_weight_decay.restype = i32
     lib.lopt_step.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, i64, ctypes.c_float, vp]
     lib.lopt_step.restype = i32
+    lib.lopt_shard_sizes.argtypes = [ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.lopt_shard_sizes.restype = i32
+    lib.lopt_shard_begin.argtypes = [vp, ctypes.POINTER(LoptTensor), ctypes.POINTER(i64), i32, i64, ctypes.c_float,
+                                     vp, vp, vp]
+    lib.lopt_shard_begin.restype = i32
+    lib.lopt_shard_middle.argtypes = [vp, vp]
+    lib.lopt_shard_middle.restype = i32
+    lib.lopt_shard_end.argtypes = [vp, vp]
+    lib.lopt_shard_end.restype = i32
     lib.lopt_check.argtypes = [vp]
     lib.lopt_check.restype = i32
     lib.lopt_feature_stats.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double)]
@@ -202,6 +212,53 @@ class LearnedOptimizer:
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         _check("lopt_step", load_library().lopt_step(self._h, pl.array, pl.n, int(t), float(lr),
                                                       ctypes.c_void_p(handle)))
+
+    # ---- row-sharded step --------------------------------------------------
+    @staticmethod
+    def shard_buffers(tensors, device=None):
+        """Exchange buffers (float64, on the GPU) of a row-sharded step."""
+        import torch
+        pl = tensors if isinstance(tensors, PreparedList) else PreparedList(
+            [t if isinstance(t, TensorState) else TensorState.from_dict(t) for t in tensors])
+        n1, n2 = ctypes.c_int64(), ctypes.c_int64()
+        _check("lopt_shard_sizes", load_library().lopt_shard_sizes(pl.array, pl.n, ctypes.byref(n1),
+                                                                    ctypes.byref(n2)))
+        dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+        return (torch.zeros(n1.value, dtype=torch.float64, device=dev),
+                torch.zeros(n2.value, dtype=torch.float64, device=dev))
+
+    @staticmethod
+    def _stream(stream):
+        import torch
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+    def shard_begin(self, tensors, global_rows, t: int, lr: float, x1, x2, stream=None) -> None:
+        pl = tensors if isinstance(tensors, PreparedList) else self.prepare(tensors)
+        gr = (ctypes.c_int64 * pl.n)(*[int(r) for r in global_rows])
+        for x in (x1, x2):
+            if not x.is_cuda or x.dtype.itemsize != 8 or not x.is_contiguous():
+                raise TypeError("exchange buffers must be contiguous CUDA float64 tensors")
+        _check("lopt_shard_begin", load_library().lopt_shard_begin(
+            self._h, pl.array, gr, pl.n, int(t), float(lr), ctypes.c_void_p(x1.data_ptr()),
+            ctypes.c_void_p(x2.data_ptr()), self._stream(stream)))
+
+    def shard_middle(self, stream=None) -> None:
+        _check("lopt_shard_middle", load_library().lopt_shard_middle(self._h, self._stream(stream)))
+
+    def shard_end(self, stream=None) -> None:
+        _check("lopt_shard_end", load_library().lopt_shard_end(self._h, self._stream(stream)))
+
+    def sharded_step(self, tensors, global_rows, t: int, lr: float, x1, x2, all_reduce,
+                     stream=None) -> None:
+        """One row-sharded step; ``all_reduce(buffer)`` sums a float64 CUDA
+        buffer over the ranks in place (e.g. torch.distributed.all_reduce)."""
+        self.shard_begin(tensors, global_rows, t, lr, x1, x2, stream)
+        all_reduce(x1)
+        self.shard_middle(stream)
+        all_reduce(x2)
+        self.shard_end(stream)
 
     def check(self) -> None:
         """Wait for the last step; raise if a kernel reported an error."""
