@@ -27,6 +27,19 @@ namespace lopt {
 namespace {
 
 constexpr int kT = kRowColThreads;
+
+// Compensated (Kahan) fp32 summation: the rounding error of each addition is
+// carried into the next one.
+struct KahanSum {
+  float sum = 0.f, comp = 0.f;
+  __device__ void add(float x) {
+    const float y = fadd(x, -comp);
+    const float t = fadd(sum, y);
+    comp = fadd(fadd(t, -sum), -y);
+    sum = t;
+  }
+  __device__ float value() const { return sum; }
+};
 constexpr int kWarps = kT / 32;
 constexpr int kRowBatch = 8;         // rows reduced together
 
@@ -244,14 +257,18 @@ __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
       xout[d.C + tid] = s;
     }
   } else if (d.vec4 && (d.C % 4 == 0)) {
+    // compensated fp32 sums (FP64 is slow on this part; the error stays a
+    // few ulp whatever the number of strips)
+    const float invRf = (float)invR;
     for (int64_t j = 4 * (int64_t)tid; j < d.C; j += 4 * (int64_t)kT) {
-      double s0 = 0.0, s1 = 0.0, s2 = 0.0, s3 = 0.0;
+      KahanSum s0, s1, s2, s3;
 #pragma unroll 8
       for (int st = 0; st < S; ++st) {
         const float4 x = __ldcg(reinterpret_cast<const float4*>(cp + (int64_t)st * d.C + j));
-        s0 += (double)x.x; s1 += (double)x.y; s2 += (double)x.z; s3 += (double)x.w;
+        s0.add(x.x); s1.add(x.y); s2.add(x.z); s3.add(x.w);
       }
-      const float H[4] = {(float)(s0 * invR), (float)(s1 * invR), (float)(s2 * invR), (float)(s3 * invR)};
+      const float H[4] = {fmul(s0.value(), invRf), fmul(s1.value(), invRf), fmul(s2.value(), invRf),
+                          fmul(s3.value(), invRf)};
 #pragma unroll
       for (int k = 0; k < 3; ++k) {
         float4* c4 = reinterpret_cast<float4*>(d.c[k] + j);
@@ -264,11 +281,12 @@ __global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
       }
     }
   } else {
+    const float invRf = (float)invR;
     for (int64_t j = tid; j < d.C; j += kT) {
-      double s = 0.0;
+      KahanSum s;
 #pragma unroll 8
-      for (int st = 0; st < S; ++st) s += (double)__ldcg(cp + (int64_t)st * d.C + j);
-      const float H = (float)(s * invR);
+      for (int st = 0; st < S; ++st) s.add(__ldcg(cp + (int64_t)st * d.C + j));
+      const float H = fmul(s.value(), invRf);
 #pragma unroll
       for (int k = 0; k < 3; ++k) {
         float* c = d.c[k] + j;
