@@ -66,12 +66,12 @@ __device__ void fold_first_layer(const StepArgs& a, int T, const TensorDesc& d, 
     for (int h = tid; h < H; h += kT) {
       double b = (double)b1[h];
       for (int s = 0; s < kTimeFeat; ++s) {
-        b += tanh(a.t / time_scale(s)) * (double)W1[(kStats + s) * H + h];
+        b += a.tau[s] * (double)W1[(kStats + s) * H + h];
       }
       out[kStats * H + h] = (float)b;
     }
   } else {
-    fold_w1_tc(H, W1, b1, a.t, out);
+    fold_w1_tc(H, W1, b1, a.tau, out);
   }
 }
 

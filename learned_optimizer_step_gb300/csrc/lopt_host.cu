@@ -456,6 +456,7 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   a.path = h->path;
   a.tc_weights = h->d_tcw;
   a.t = (double)t;
+  for (int k = 0; k < kTimeFeat; ++k) a.tau[k] = std::tanh((double)t / time_scale(k));
   a.lr = lr;
   a.wd = h->weight_decay;
   a.status = h->d_status;
@@ -554,6 +555,7 @@ int lopt_shard_begin(lopt_handle h, const lopt_tensor* tensors, const int64_t* g
   a.path = h->path;
   a.tc_weights = h->d_tcw;
   a.t = (double)t;
+  for (int k = 0; k < kTimeFeat; ++k) a.tau[k] = std::tanh((double)t / time_scale(k));
   a.lr = lr;
   a.wd = h->weight_decay;
   a.status = h->d_status;

@@ -95,6 +95,7 @@ struct StepArgs {
   int32_t           path;        // LOPT_MLP_*
   const void*       tc_weights;  // per-set packed FP16 B operands (tensor-core path)
   double            t;           // step count
+  double            tau[kTimeFeat];   // tanh(t / x_s), computed once on the host
   float             lr;
   float             wd;          // decoupled weight decay: p -= lr * (update + wd * p)
   // Row-sharded steps only (null otherwise): this rank's sums that the ranks

@@ -298,7 +298,7 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
 //   B[n][k] = W1[k][n] (k < 28),  b1[n] + sum_s tau_s W1[28+s][n] (k = 28),
 //   0 otherwise or for padded units n >= hp.
 // (The normalisation scales are applied to the features themselves.)
-__device__ inline void fold_w1_tc(int hp, const float* W1, const float* b1, double t, float* out) {
+__device__ inline void fold_w1_tc(int hp, const float* W1, const float* b1, const double* tau, float* out) {
   const int np = tc_np(hp);
   __half* o = reinterpret_cast<__half*>(out);
   for (int x = threadIdx.x; x < np * 32; x += blockDim.x) {
@@ -309,7 +309,7 @@ __device__ inline void fold_w1_tc(int hp, const float* W1, const float* b1, doub
         v = (double)W1[k * hp + n];
       } else if (k == kStats) {
         v = (double)b1[n];
-        for (int s = 0; s < kTimeFeat; ++s) v += tanh(t / time_scale(s)) * (double)W1[(kStats + s) * hp + n];
+        for (int s = 0; s < kTimeFeat; ++s) v += tau[s] * (double)W1[(kStats + s) * hp + n];
       }
     }
     o[f16_off(n, k, 32)] = __float2half_rn((float)v);
