@@ -249,14 +249,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   const int32_t u_first = (int32_t)((int64_t)blockIdx.x * U / gridDim.x);
   const int32_t u_last = (int32_t)((int64_t)(blockIdx.x + 1) * U / gridDim.x);
 
-  for (int32_t u0 = u_first; u0 < u_last;) {
-    // ---- session set-up: tiles sharing one weight set --------------------------
+  // ---- sessions: maximal runs of tiles that share one MLP weight set --------
+  // Every role runs the same sequence of sessions and meets the same
+  // barriers; set-up and tear-down of a session are common to all.
+  auto begin_session = [&](int32_t u0, int32_t& u1, int32_t& K) -> bool {
     if (tid == 0) {
       const int wset = a.desc[a.units[u0].tensor].wset;
-      int32_t u1 = u0, K = 0;
-      while (u1 < u_last && a.desc[a.units[u1].tensor].wset == wset) K += unit_tiles(a, u1++);
-      info[0] = u1;
-      info[1] = K;
+      int32_t e = u0, n = 0;
+      while (e < u_last && a.desc[a.units[e].tensor].wset == wset) n += unit_tiles(a, e++);
+      info[0] = e;
+      info[1] = n;
       for (int r = 0; r < R; ++r) {
         mbar_init(ring_full + r, 1);
         mbar_init(stage_done + r, kStageUsers);
@@ -280,329 +282,347 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
     }
     fence_proxy_async();
     __syncthreads();
-    const int32_t u1 = info[0], K = info[1];
-    if (*abort_flag) break;
+    u1 = info[0];
+    K = info[1];
+    return !*abort_flag;
+  };
+  auto sessions = [&](auto&& role) {
+    for (int32_t u0 = u_first, u1 = 0, K = 0; u0 < u_last; u0 = u1) {
+      if (!begin_session(u0, u1, K)) break;
+      role(u0, u1, K);
+      // ---- session end: every role has finished its tiles
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+  };
 
-    if (warp == kProducerWarp) {
-      // ------------------------------ producer -------------------------------
-      // Lane q < 6 moves array q of every stage.  Before a slot is loaded
-      // again, the stage it held is written back (p, m0..2, v) once every
-      // feature and epilogue thread has left it.
-      auto write_back = [&](int st) {
-        const StageRec r = rec[st];
-        if (r.bytes != 0 && lane < kArrays && lane != 1) {
-          bulk_s2g(stage_array(a.desc[r.tensor], lane) + r.e0, ring + st * (kArrays * kStageElems) + lane * kStageElems,
-                   r.bytes);
-          bulk_commit();
-          bulk_wait_read_all();   // the slot may be refilled once its contents have been read
-        }
-        __syncwarp();
-      };
-      int32_t n = 0;      // stages issued
-      int st = 0;         // slot of stage n
-      uint32_t ph = 0;    // its round parity
-      bool stop = false;
-      for (int32_t u = u0; u < u1 && !stop; ++u) {
-        const Unit x = a.units[u];
-        const TensorDesc& d = a.desc[x.tensor];
-        const bool stg = staged(d);
-        const int64_t ub = (int64_t)x.local * kApplyChunk;
-        const int64_t ue = min(d.N, ub + kApplyChunk);
-        const float* src = stage_array(d, lane < kArrays ? lane : 0);
-        for (int64_t e0 = ub; e0 < ue; e0 += kStageElems) {
-          if (n >= R) {   // the slot's previous stage: round ph ^ 1
-            if (!mbar_wait_or_abort(stage_done + st, ph ^ 1u, kWaitNs, abort_flag)) {
+  if (warp >= kProducerWarp) {
+    sessions([&](int32_t u0, int32_t u1, int32_t K) {
+      if (warp == kProducerWarp) {
+
+          // ------------------------------ producer -------------------------------
+          // Lane q < 6 moves array q of every stage.  Before a slot is loaded
+          // again, the stage it held is written back (p, m0..2, v) once every
+          // feature and epilogue thread has left it.
+          auto write_back = [&](int st) {
+            const StageRec r = rec[st];
+            if (r.bytes != 0 && lane < kArrays && lane != 1) {
+              bulk_s2g(stage_array(a.desc[r.tensor], lane) + r.e0, ring + st * (kArrays * kStageElems) + lane * kStageElems,
+                       r.bytes);
+              bulk_commit();
+              bulk_wait_read_all();   // the slot may be refilled once its contents have been read
+            }
+            __syncwarp();
+          };
+          int32_t n = 0;      // stages issued
+          int st = 0;         // slot of stage n
+          uint32_t ph = 0;    // its round parity
+          bool stop = false;
+          for (int32_t u = u0; u < u1 && !stop; ++u) {
+            const Unit x = a.units[u];
+            const TensorDesc& d = a.desc[x.tensor];
+            const bool stg = staged(d);
+            const int64_t ub = (int64_t)x.local * kApplyChunk;
+            const int64_t ue = min(d.N, ub + kApplyChunk);
+            const float* src = stage_array(d, lane < kArrays ? lane : 0);
+            for (int64_t e0 = ub; e0 < ue; e0 += kStageElems) {
+              if (n >= R) {   // the slot's previous stage: round ph ^ 1
+                if (!mbar_wait_or_abort(stage_done + st, ph ^ 1u, kWaitNs, abort_flag)) {
+                  stop = true;
+                  break;
+                }
+                write_back(st);
+              }
+              const uint32_t bytes = (uint32_t)(min((int64_t)kStageElems, ue - e0) * 4);
+              StageRec& rc = rec[st];
+              if (lane < kStats) rc.sc[lane] = a.aux[x.tensor].scale[lane];
+              else if (lane < kStats + 3) rc.inv_rho[lane - kStats] = a.aux[x.tensor].inv_rho[lane - kStats];
+              else if (lane == 31) {
+                rc.tensor = x.tensor;
+                rc.e0 = e0;
+                rc.i0 = e0 / d.C;
+                rc.j0 = (int32_t)(e0 - rc.i0 * d.C);
+                rc.C = (int32_t)d.C;
+                rc.invC = 1.0f / (float)d.C;
+                rc.bytes = stg ? bytes : 0u;
+              }
+              if (lane < 3) rc.c[lane] = d.c[lane];
+              else if (lane < 6) rc.r[lane - 3] = d.r[lane - 3];
+              __syncwarp();
+              if (lane == 0) {
+                if (stg) mbar_arrive_expect_tx(ring_full + st, kArrays * bytes);
+                else mbar_arrive(ring_full + st);
+              }
+              __syncwarp();
+              if (stg && lane < kArrays)
+                bulk_g2s(ring + st * (kArrays * kStageElems) + lane * kStageElems, src + e0, bytes, ring_full + st);
+              ++n;
+              if (++st == R) { st = 0; ph ^= 1u; }
+            }
+          }
+          // the stages still in the ring, oldest first
+          for (int32_t x = (n > R ? n - R : 0); x < n && !stop; ++x) {
+            const int xs = x % R;
+            if (!mbar_wait_or_abort(stage_done + xs, (uint32_t)((x / R) & 1), kWaitNs, abort_flag)) {
               stop = true;
               break;
             }
-            write_back(st);
+            write_back(xs);
           }
-          const uint32_t bytes = (uint32_t)(min((int64_t)kStageElems, ue - e0) * 4);
-          StageRec& rc = rec[st];
-          if (lane < kStats) rc.sc[lane] = a.aux[x.tensor].scale[lane];
-          else if (lane < kStats + 3) rc.inv_rho[lane - kStats] = a.aux[x.tensor].inv_rho[lane - kStats];
-          else if (lane == 31) {
-            rc.tensor = x.tensor;
-            rc.e0 = e0;
-            rc.i0 = e0 / d.C;
-            rc.j0 = (int32_t)(e0 - rc.i0 * d.C);
-            rc.C = (int32_t)d.C;
-            rc.invC = 1.0f / (float)d.C;
-            rc.bytes = stg ? bytes : 0u;
+          if (stop) {   // let loads already issued land before teardown
+            for (int32_t x = (n > R ? n - R : 0); x < n; ++x)
+              mbar_drain(ring_full + x % R, (uint32_t)((x / R) & 1), kWaitNs / 10);
           }
-          if (lane < 3) rc.c[lane] = d.c[lane];
-          else if (lane < 6) rc.r[lane - 3] = d.r[lane - 3];
-          __syncwarp();
+          bulk_wait_all();   // every write-back complete before the session ends
+      } else if (warp == kMma1Warp || warp == kMma2Warp) {
+
+          // ------------------------------ MMA issuers ----------------------------
+          // One thread per layer: layer 1 of tile k once its A operand is in
+          // tensor memory, committed to done1[k]; layer 2 of tile k once its A
+          // operand and b2 preset are, committed to done2[k].
           if (lane == 0) {
-            if (stg) mbar_arrive_expect_tx(ring_full + st, kArrays * bytes);
-            else mbar_arrive(ring_full + st);
+            const bool l1 = warp == kMma1Warp;
+            const uint64_t dB = l1 ? smem_desc(s_base + G::oB1, 128, G::SBO1) : smem_desc(s_base + G::oB2, 128, G::SBO);
+            uint64_t* const full = l1 ? a1_full : a2_full;
+            uint64_t* const fin = l1 ? done1 : done2;
+            const int ksteps = l1 ? 2 : NP / 16;   // K-steps of 16 FP16 values (8 A columns)
+            int s = 0;
+            uint32_t ph = 0;
+            int k = 0;
+            for (; k < K; ++k) {
+              if (!mbar_wait_or_abort(full + s, ph, kWaitNs, abort_flag)) break;
+              tc_fence_after();
+              const uint32_t d = tmem + s * G::SlotCols;
+              // layer 1 overwrites its accumulator; layer 2 adds onto the b2 preset
+              mma_f16_ts(d, d + NP, dB, G::ID12, l1 ? 0u : 1u);
+              if (ksteps > 1) mma_f16_ts(d, d + NP + 8, dB + 16, G::ID12, 1u);
+              mma_commit(fin + (k & (kDone - 1)));   // tracks every MMA of this thread so far
+              if (++s == S) { s = 0; ph ^= 1u; }
+            }
+            // nothing of ours may still be running when the session ends
+            if (k > 0) mbar_drain(fin + ((k - 1) & (kDone - 1)), (uint32_t)(((k - 1) / kDone) & 1), kWaitNs / 10);
           }
-          __syncwarp();
-          if (stg && lane < kArrays)
-            bulk_g2s(ring + st * (kArrays * kStageElems) + lane * kStageElems, src + e0, bytes, ring_full + st);
-          ++n;
-          if (++st == R) { st = 0; ph ^= 1u; }
+      }
+    });
+  } else if (warp >= kFeatWarp0) {
+    sessions([&](int32_t u0, int32_t u1, int32_t K) {
+
+        // --------------------------- feature warpgroups ------------------------
+        // Group grp owns the stages n with n % 2 == grp and builds the A
+        // operand of layer 1 for each of their tiles in order.
+        const int grp = (warp - kFeatWarp0) >> 2;
+        const int t = tid - 32 * kFeatWarp0 - 128 * grp;
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        StageIter si;
+        si.init(a.units, a.desc, u0, u1);
+        bool ok = true;
+        for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
+          if (ns % kFeatGroups != grp) continue;
+          if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
+          const StageRec& rc = rec[si.st];
+          const bool stg = rc.bytes != 0;
+          float* const sbase = ring + si.st * (kArrays * kStageElems);
+          const int ntl = (si.n + kTile - 1) / kTile;
+          int s = si.k0 % S;                          // slot of the stage's first tile
+          uint32_t sph = (uint32_t)((si.k0 / S) & 1);  // its round parity
+          for (int j = 0; j < ntl; ++j) {
+            const int x = j * kTile + t;                 // element offset in the stage
+            const int xi = min(x, si.n - 1);             // past the end: index math of the last element
+            float p, g, m[3], v;
+            if (stg) {   // elements past the end read and write unused stage words
+              p = sbase[x]; g = sbase[kStageElems + x]; m[0] = sbase[2 * kStageElems + x];
+              m[1] = sbase[3 * kStageElems + x]; m[2] = sbase[4 * kStageElems + x]; v = sbase[5 * kStageElems + x];
+            } else {
+              const TensorDesc& d = a.desc[rc.tensor];
+              const int64_t e = rc.e0 + xi;
+              p = d.p[e]; g = __ldg(d.g + e); v = d.v[e];
+#pragma unroll
+              for (int q = 0; q < 3; ++q) m[q] = d.m[q][e];
+            }
+            // row and column of the element: j0 + xi < C + kStageElems, so a
+            // float quotient is exact to within one
+            const uint32_t C = (uint32_t)rc.C;
+            int64_t i = rc.i0;
+            uint32_t jc = (uint32_t)rc.j0 + (uint32_t)xi;
+            if (jc >= C) {
+              uint32_t q = (uint32_t)((float)jc * rc.invC);
+              int32_t rem = (int32_t)(jc - q * C);
+              if (rem < 0) { --q; rem += (int32_t)C; }
+              else if (rem >= (int32_t)C) { ++q; rem -= (int32_t)C; }
+              i += q;
+              jc = (uint32_t)rem;
+            }
+            float c[3], r[3];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+              c[q] = __ldg(rc.c[q] + jc);
+              r[q] = __ldg(rc.r[q] + i);
+            }
+            float inv_rho[3];
+#pragma unroll
+            for (int q = 0; q < 3; ++q) inv_rho[q] = rc.inv_rho[q];
+            const RowTerms rt = row_terms_of(r, inv_rho);
+            float f[kStats];
+            lopt_features(p, g, m, v, rt, c, f);
+            if (stg) {
+              sbase[2 * kStageElems + x] = m[0]; sbase[3 * kStageElems + x] = m[1];
+              sbase[4 * kStageElems + x] = m[2]; sbase[5 * kStageElems + x] = v;
+            } else if (x < si.n) {
+              const TensorDesc& d = a.desc[rc.tensor];
+              const int64_t e = rc.e0 + x;
+#pragma unroll
+              for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
+              d.v[e] = v;
+            }
+            // normalised features, FP16, into this lane's row of the slot's A
+            // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
+            uint32_t av[16];
+            const float4* sc4 = reinterpret_cast<const float4*>(rc.sc);
+#pragma unroll
+            for (int q = 0; q < 7; ++q) {
+              const float4 sq = sc4[q];
+              av[2 * q] = f16x2(f[4 * q] * sq.x, f[4 * q + 1] * sq.y);
+              av[2 * q + 1] = f16x2(f[4 * q + 2] * sq.z, f[4 * q + 3] * sq.w);
+            }
+            av[14] = 0x00003C00u;   // 1.0h, 0
+            av[15] = 0u;
+            // the tile's slot is needed only now: loads and arithmetic above
+            // overlap the wait for it
+            if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) { ok = false; break; }
+            tmem_st16(t_lane + s * G::SlotCols + NP, av);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(a1_full + s);
+            if (++s == S) { s = 0; sph ^= 1u; }
+          }
+          if (!ok) break;
+          fence_proxy_async();   // m, v in the stage, before its write-back
+          mbar_arrive(stage_done + si.st);
         }
-      }
-      // the stages still in the ring, oldest first
-      for (int32_t x = (n > R ? n - R : 0); x < n && !stop; ++x) {
-        const int xs = x % R;
-        if (!mbar_wait_or_abort(stage_done + xs, (uint32_t)((x / R) & 1), kWaitNs, abort_flag)) {
-          stop = true;
-          break;
-        }
-        write_back(xs);
-      }
-      if (stop) {   // let loads already issued land before teardown
-        for (int32_t x = (n > R ? n - R : 0); x < n; ++x)
-          mbar_drain(ring_full + x % R, (uint32_t)((x / R) & 1), kWaitNs / 10);
-      }
-      bulk_wait_all();   // every write-back complete before the session ends
-    } else if (warp >= kFeatWarp0 && warp < kProducerWarp) {
-      // --------------------------- feature warpgroups ------------------------
-      // Group grp owns the stages n with n % 2 == grp and builds the A
-      // operand of layer 1 for each of their tiles in order.
-      const int grp = (warp - kFeatWarp0) >> 2;
-      const int t = tid - 32 * kFeatWarp0 - 128 * grp;
-      const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      StageIter si;
-      si.init(a.units, a.desc, u0, u1);
-      bool ok = true;
-      for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
-        if (ns % kFeatGroups != grp) continue;
-        if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
-        const StageRec& rc = rec[si.st];
-        const bool stg = rc.bytes != 0;
-        float* const sbase = ring + si.st * (kArrays * kStageElems);
-        const int ntl = (si.n + kTile - 1) / kTile;
-        int s = si.k0 % S;                          // slot of the stage's first tile
-        uint32_t sph = (uint32_t)((si.k0 / S) & 1);  // its round parity
-        for (int j = 0; j < ntl; ++j) {
-          const int x = j * kTile + t;                 // element offset in the stage
-          const int xi = min(x, si.n - 1);             // past the end: index math of the last element
-          float p, g, m[3], v;
-          if (stg) {   // elements past the end read and write unused stage words
-            p = sbase[x]; g = sbase[kStageElems + x]; m[0] = sbase[2 * kStageElems + x];
-            m[1] = sbase[3 * kStageElems + x]; m[2] = sbase[4 * kStageElems + x]; v = sbase[5 * kStageElems + x];
-          } else {
-            const TensorDesc& d = a.desc[rc.tensor];
-            const int64_t e = rc.e0 + xi;
-            p = d.p[e]; g = __ldg(d.g + e); v = d.v[e];
+    });
+  } else {
+    sessions([&](int32_t u0, int32_t u1, int32_t K) {
+
+        // ------------------------------ epilogue -------------------------------
+        // Group h owns the stages n with n % 2 == h.  For a stage it first
+        // finishes layer 1 of every tile (ReLU, FP16 A operand of layer 2, b2
+        // preset of its accumulator), then the rest of every tile (ReLU(h2),
+        // output layer, update of p in the stage).
+        const int h = warp >> 2;
+        const int t = tid - 128 * h;
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
+        const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
+        const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
+        const float lr = a.lr, wd = a.wd;
+        StageIter si;
+        si.init(a.units, a.desc, u0, u1);
+        bool ok = true;
+        for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
+          if (ns % kEpiGroups != h) continue;
+          // the stage's record (written by the producer before it was loaded)
+          if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
+          const int ntl = (si.n + kTile - 1) / kTile;
+          const int s0 = si.k0 % S;
+          // ---- layer 1 of every tile
+          int s = s0;
+          for (int j = 0; j < ntl; ++j) {
+            const int32_t k = si.k0 + j;
+            if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t col = t_lane + s * G::SlotCols;
+            uint32_t av[16];
+            {
+              uint32_t h1[NP];
+              tmem_ld_row<NP>(col, h1);
+              tmem_wait_ld();
+              pack_relu_row<NP>(h1, av);
+            }
+            tmem_st16(col + NP, av);
+            uint32_t b2[NP];
 #pragma unroll
-            for (int q = 0; q < 3; ++q) m[q] = d.m[q][e];
+            for (int q = 0; q < NP; q += 4) {
+              const float4 b = *reinterpret_cast<const float4*>(aux + q);
+              b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
+              b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
+            }
+            tmem_st_row<NP>(col, b2);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(a2_full + s);
+            if (++s == S) s = 0;
           }
-          // row and column of the element: j0 + xi < C + kStageElems, so a
-          // float quotient is exact to within one
-          const uint32_t C = (uint32_t)rc.C;
-          int64_t i = rc.i0;
-          uint32_t jc = (uint32_t)rc.j0 + (uint32_t)xi;
-          if (jc >= C) {
-            uint32_t q = (uint32_t)((float)jc * rc.invC);
-            int32_t rem = (int32_t)(jc - q * C);
-            if (rem < 0) { --q; rem += (int32_t)C; }
-            else if (rem >= (int32_t)C) { ++q; rem -= (int32_t)C; }
-            i += q;
-            jc = (uint32_t)rem;
-          }
-          float c[3], r[3];
-#pragma unroll
-          for (int q = 0; q < 3; ++q) {
-            c[q] = __ldg(rc.c[q] + jc);
-            r[q] = __ldg(rc.r[q] + i);
-          }
-          float inv_rho[3];
-#pragma unroll
-          for (int q = 0; q < 3; ++q) inv_rho[q] = rc.inv_rho[q];
-          const RowTerms rt = row_terms_of(r, inv_rho);
-          float f[kStats];
-          lopt_features(p, g, m, v, rt, c, f);
-          if (stg) {
-            sbase[2 * kStageElems + x] = m[0]; sbase[3 * kStageElems + x] = m[1];
-            sbase[4 * kStageElems + x] = m[2]; sbase[5 * kStageElems + x] = v;
-          } else if (x < si.n) {
-            const TensorDesc& d = a.desc[rc.tensor];
-            const int64_t e = rc.e0 + x;
-#pragma unroll
-            for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
-            d.v[e] = v;
-          }
-          // normalised features, FP16, into this lane's row of the slot's A
-          // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
-          uint32_t av[16];
-          const float4* sc4 = reinterpret_cast<const float4*>(rc.sc);
-#pragma unroll
-          for (int q = 0; q < 7; ++q) {
-            const float4 sq = sc4[q];
-            av[2 * q] = f16x2(f[4 * q] * sq.x, f[4 * q + 1] * sq.y);
-            av[2 * q + 1] = f16x2(f[4 * q + 2] * sq.z, f[4 * q + 3] * sq.w);
-          }
-          av[14] = 0x00003C00u;   // 1.0h, 0
-          av[15] = 0u;
-          // the tile's slot is needed only now: loads and arithmetic above
-          // overlap the wait for it
-          if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) { ok = false; break; }
-          tmem_st16(t_lane + s * G::SlotCols + NP, av);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(a1_full + s);
-          if (++s == S) { s = 0; sph ^= 1u; }
-        }
-        if (!ok) break;
-        fence_proxy_async();   // m, v in the stage, before its write-back
-        mbar_arrive(stage_done + si.st);
-      }
-    } else if (warp == kMma1Warp || warp == kMma2Warp) {
-      // ------------------------------ MMA issuers ----------------------------
-      // One thread per layer: layer 1 of tile k once its A operand is in
-      // tensor memory, committed to done1[k]; layer 2 of tile k once its A
-      // operand and b2 preset are, committed to done2[k].
-      if (lane == 0) {
-        const bool l1 = warp == kMma1Warp;
-        const uint64_t dB = l1 ? smem_desc(s_base + G::oB1, 128, G::SBO1) : smem_desc(s_base + G::oB2, 128, G::SBO);
-        uint64_t* const full = l1 ? a1_full : a2_full;
-        uint64_t* const fin = l1 ? done1 : done2;
-        const int ksteps = l1 ? 2 : NP / 16;   // K-steps of 16 FP16 values (8 A columns)
-        int s = 0;
-        uint32_t ph = 0;
-        int k = 0;
-        for (; k < K; ++k) {
-          if (!mbar_wait_or_abort(full + s, ph, kWaitNs, abort_flag)) break;
-          tc_fence_after();
-          const uint32_t d = tmem + s * G::SlotCols;
-          // layer 1 overwrites its accumulator; layer 2 adds onto the b2 preset
-          mma_f16_ts(d, d + NP, dB, G::ID12, l1 ? 0u : 1u);
-          if (ksteps > 1) mma_f16_ts(d, d + NP + 8, dB + 16, G::ID12, 1u);
-          mma_commit(fin + (k & (kDone - 1)));   // tracks every MMA of this thread so far
-          if (++s == S) { s = 0; ph ^= 1u; }
-        }
-        // nothing of ours may still be running when the session ends
-        if (k > 0) mbar_drain(fin + ((k - 1) & (kDone - 1)), (uint32_t)(((k - 1) / kDone) & 1), kWaitNs / 10);
-      }
-    } else if (warp < kFeatWarp0) {
-      // ------------------------------ epilogue -------------------------------
-      // Group h owns the stages n with n % 2 == h.  For a stage it first
-      // finishes layer 1 of every tile (ReLU, FP16 A operand of layer 2, b2
-      // preset of its accumulator), then the rest of every tile (ReLU(h2),
-      // output layer, update of p in the stage).
-      const int h = warp >> 2;
-      const int t = tid - 128 * h;
-      const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-      const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
-      const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
-      const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
-      const float lr = a.lr, wd = a.wd;
-      StageIter si;
-      si.init(a.units, a.desc, u0, u1);
-      bool ok = true;
-      for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
-        if (ns % kEpiGroups != h) continue;
-        // the stage's record (written by the producer before it was loaded)
-        if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
-        const int ntl = (si.n + kTile - 1) / kTile;
-        const int s0 = si.k0 % S;
-        // ---- layer 1 of every tile
-        int s = s0;
-        for (int j = 0; j < ntl; ++j) {
-          const int32_t k = si.k0 + j;
-          if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t col = t_lane + s * G::SlotCols;
-          uint32_t av[16];
-          {
-            uint32_t h1[NP];
-            tmem_ld_row<NP>(col, h1);
+          if (!ok) break;
+          // ---- the rest of every tile; a slot is freed as soon as h2 is read
+          const StageRec& rc = rec[si.st];
+          const bool stg = rc.bytes != 0;
+          float* const pst = ring + si.st * (kArrays * kStageElems);
+          s = s0;
+          for (int j = 0; j < ntl; ++j) {
+            const int32_t k = si.k0 + j;
+            if (!mbar_wait_or_abort(done2 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint32_t h2[NP];
+            tmem_ld_row<NP>(t_lane + s * G::SlotCols, h2);
             tmem_wait_ld();
-            pack_relu_row<NP>(h1, av);
-          }
-          tmem_st16(col + NP, av);
-          uint32_t b2[NP];
+            tc_fence_before();
+            mbar_arrive(slot_empty + s);
+            if (++s == S) s = 0;
+            // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3, in
+            // chunks of 8 hidden units whose weights are loaded one chunk
+            // ahead (shared-memory latency off the FMA chains)
+            constexpr int kCh = NP / 8;
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};   // (o0, o1) x 2 chains
+            float4 wcur[4], wnext[4];
 #pragma unroll
-          for (int q = 0; q < NP; q += 4) {
-            const float4 b = *reinterpret_cast<const float4*>(aux + q);
-            b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
-            b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
+            for (int q = 0; q < 4; ++q) wcur[q] = w3[q];
+#pragma unroll
+            for (int ch = 0; ch < kCh; ++ch) {
+              if (ch + 1 < kCh) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wnext[q] = w3[4 * (ch + 1) + q];
+              }
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int u = 8 * ch + 2 * q;
+                const float2 hr = make_float2(fmaxf(__uint_as_float(h2[u]), 0.f),
+                                              fmaxf(__uint_as_float(h2[u + 1]), 0.f));
+                acc[(q & 1) * 2] = __ffma2_rn(hr, make_float2(wcur[q].x, wcur[q].y), acc[(q & 1) * 2]);
+                acc[(q & 1) * 2 + 1] = __ffma2_rn(hr, make_float2(wcur[q].z, wcur[q].w), acc[(q & 1) * 2 + 1]);
+              }
+              if (ch + 1 < kCh) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wcur[q] = wnext[q];
+              }
+            }
+            const float o0 = (acc[0].x + acc[0].y) + (acc[2].x + acc[2].y) + b30;
+            const float o1 = (acc[1].x + acc[1].y) + (acc[3].x + acc[3].y) + b31;
+            // exp(x) = 2^(x log2 e) with the PTX ex2.approx instruction
+            // (relative error below 2^-22); here |x| = |o1| * 1e-3 is small
+            float ex;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
+            const float upd = o0 * ex * kOutScale;
+            const int x = j * kTile + t;
+            if (stg) {   // past the end: an unused stage word
+              pst[x] = pst[x] - lr * (upd + wd * pst[x]);
+            } else if (x < si.n) {
+              float* pp = a.desc[rc.tensor].p + (rc.e0 + x);
+              *pp = *pp - lr * (upd + wd * *pp);
+            }
           }
-          tmem_st_row<NP>(col, b2);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(a2_full + s);
-          if (++s == S) s = 0;
+          if (!ok) break;
+          fence_proxy_async();   // p in the stage, before its write-back
+          mbar_arrive(stage_done + si.st);
         }
-        if (!ok) break;
-        // ---- the rest of every tile; a slot is freed as soon as h2 is read
-        const StageRec& rc = rec[si.st];
-        const bool stg = rc.bytes != 0;
-        float* const pst = ring + si.st * (kArrays * kStageElems);
-        s = s0;
-        for (int j = 0; j < ntl; ++j) {
-          const int32_t k = si.k0 + j;
-          if (!mbar_wait_or_abort(done2 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint32_t h2[NP];
-          tmem_ld_row<NP>(t_lane + s * G::SlotCols, h2);
-          tmem_wait_ld();
-          tc_fence_before();
-          mbar_arrive(slot_empty + s);
-          if (++s == S) s = 0;
-          // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3, in
-          // chunks of 8 hidden units whose weights are loaded one chunk
-          // ahead (shared-memory latency off the FMA chains)
-          constexpr int kCh = NP / 8;
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                           make_float2(0.f, 0.f)};   // (o0, o1) x 2 chains
-          float4 wcur[4], wnext[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) wcur[q] = w3[q];
-#pragma unroll
-          for (int ch = 0; ch < kCh; ++ch) {
-            if (ch + 1 < kCh) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) wnext[q] = w3[4 * (ch + 1) + q];
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int u = 8 * ch + 2 * q;
-              const float2 hr = make_float2(fmaxf(__uint_as_float(h2[u]), 0.f),
-                                            fmaxf(__uint_as_float(h2[u + 1]), 0.f));
-              acc[(q & 1) * 2] = __ffma2_rn(hr, make_float2(wcur[q].x, wcur[q].y), acc[(q & 1) * 2]);
-              acc[(q & 1) * 2 + 1] = __ffma2_rn(hr, make_float2(wcur[q].z, wcur[q].w), acc[(q & 1) * 2 + 1]);
-            }
-            if (ch + 1 < kCh) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) wcur[q] = wnext[q];
-            }
-          }
-          const float o0 = (acc[0].x + acc[0].y) + (acc[2].x + acc[2].y) + b30;
-          const float o1 = (acc[1].x + acc[1].y) + (acc[3].x + acc[3].y) + b31;
-          // exp(x) = 2^(x log2 e) with the PTX ex2.approx instruction
-          // (relative error below 2^-22); here |x| = |o1| * 1e-3 is small
-          float ex;
-          asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
-          const float upd = o0 * ex * kOutScale;
-          const int x = j * kTile + t;
-          if (stg) {   // past the end: an unused stage word
-            pst[x] = pst[x] - lr * (upd + wd * pst[x]);
-          } else if (x < si.n) {
-            float* pp = a.desc[rc.tensor].p + (rc.e0 + x);
-            *pp = *pp - lr * (upd + wd * *pp);
-          }
-        }
-        if (!ok) break;
-        fence_proxy_async();   // p in the stage, before its write-back
-        mbar_arrive(stage_done + si.st);
-      }
-    }
-    // ---- session end: every role has finished its tiles --------------------
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    u0 = u1;
+    });
   }
 
   // ------------------------------- teardown ----------------------------------
