@@ -133,22 +133,36 @@ __device__ void strip_rows_pass(const TensorDesc& d, int64_t r0, int nrows, floa
       for (int q = 0; q < W; ++q) col[v][q] = 0.f;
     for (int row = warp; row < nrows; row += kWarps) {
       const float* src = d.g + (r0 + row) * C + c0;
-      float rs = 0.f;
+      // all loads of the row segment first, so that they are in flight
+      // together: a column past the end reads the segment's first column
+      // (in bounds) and counts as zero
+      float x[kColVec][W];
 #pragma unroll
       for (int v = 0; v < kColVec; ++v) {
         const int64_t j = (int64_t)(v * 32 + lane) * W;   // column offset in the segment
+        const int64_t js = c0 + j < C ? j : 0;
+        if constexpr (W == 4) {
+          const float4 y = __ldg(reinterpret_cast<const float4*>(src + js));
+          x[v][0] = y.x; x[v][1] = y.y; x[v][2] = y.z; x[v][3] = y.w;
+        } else {
+          x[v][0] = __ldg(src + js);
+        }
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int v = 0; v < kColVec; ++v) {
+        const int64_t j = (int64_t)(v * 32 + lane) * W;
         if (c0 + j < C) {
           if constexpr (W == 4) {
-            const float4 x = __ldg(reinterpret_cast<const float4*>(src + j));
-            const float s0 = fmul(x.x, x.x), s1 = fmul(x.y, x.y), s2 = fmul(x.z, x.z), s3 = fmul(x.w, x.w);
+            const float s0 = fmul(x[v][0], x[v][0]), s1 = fmul(x[v][1], x[v][1]);
+            const float s2 = fmul(x[v][2], x[v][2]), s3 = fmul(x[v][3], x[v][3]);
             col[v][0] = fadd(col[v][0], s0);
             col[v][1] = fadd(col[v][1], s1);
             col[v][2] = fadd(col[v][2], s2);
             col[v][3] = fadd(col[v][3], s3);
             rs = fadd(rs, fadd(fadd(s0, s1), fadd(s2, s3)));
           } else {
-            const float x = __ldg(src + j);
-            const float s0 = fmul(x, x);
+            const float s0 = fmul(x[v][0], x[v][0]);
             col[v][0] = fadd(col[v][0], s0);
             rs = fadd(rs, s0);
           }
