@@ -115,7 +115,7 @@ __device__ void strip_pass(const TensorDesc& d, int64_t r0, int nrows, float* co
 // added to rowacc by that warp alone, and each lane keeps the column sums
 // of its columns in registers until the warps' column sums are combined in
 // warp order.  Same results in every run: every sum has a fixed order.
-constexpr int kColVec = 8;                 // vectors of W columns per lane and segment
+constexpr int kColVec = 4;                 // vectors of W columns per lane and segment
 
 template <int W>
 __device__ void strip_rows_pass(const TensorDesc& d, int64_t r0, int nrows, float* colpart_strip,
@@ -188,10 +188,10 @@ __device__ void strip_rows_pass(const TensorDesc& d, int64_t r0, int nrows, floa
   }
 }
 
-__global__ void __launch_bounds__(kT) k_rowcol(StepArgs a) {
+__global__ void __launch_bounds__(kT, 4) k_rowcol(StepArgs a) {   // 4 blocks per SM
   __shared__ float rowacc[kMaxStripRows];
   __shared__ float wsum[2][kWarps][kRowBatch];
-  __shared__ __align__(16) float colsum[kWarps * 32 * 4 * kColVec];   // 32 KB
+  __shared__ __align__(16) float colsum[kWarps * 32 * 4 * kColVec];   // 16 KB
   __shared__ double red[kWarps][3];
   __shared__ int is_last;
 

@@ -98,13 +98,23 @@ __global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per
     int64_t e = e0 + 4 * (int64_t)tid;
     if (e < e1) {
       RowColWalker w(e, 4 * (int64_t)kT, d.C);
+      // the element arrays of the next step are loaded before this step's
+      // arithmetic, so that a thread always has loads in flight (the last
+      // step reloads its own elements)
+      float4 p4 = __ldg(reinterpret_cast<const float4*>(d.p + e));
+      float4 g4 = __ldg(reinterpret_cast<const float4*>(d.g + e));
+      float4 a4 = __ldg(reinterpret_cast<const float4*>(d.m[0] + e));
+      float4 b4 = __ldg(reinterpret_cast<const float4*>(d.m[1] + e));
+      float4 c4 = __ldg(reinterpret_cast<const float4*>(d.m[2] + e));
+      float4 v4 = __ldg(reinterpret_cast<const float4*>(d.v + e));
       for (; e < e1; e += 4 * (int64_t)kT, w.advance()) {
-        const float4 p4 = __ldg(reinterpret_cast<const float4*>(d.p + e));
-        const float4 g4 = __ldg(reinterpret_cast<const float4*>(d.g + e));
-        const float4 a4 = __ldg(reinterpret_cast<const float4*>(d.m[0] + e));
-        const float4 b4 = __ldg(reinterpret_cast<const float4*>(d.m[1] + e));
-        const float4 c4 = __ldg(reinterpret_cast<const float4*>(d.m[2] + e));
-        const float4 v4 = __ldg(reinterpret_cast<const float4*>(d.v + e));
+        const int64_t en = e + 4 * (int64_t)kT < e1 ? e + 4 * (int64_t)kT : e;
+        const float4 np4 = __ldg(reinterpret_cast<const float4*>(d.p + en));
+        const float4 ng4 = __ldg(reinterpret_cast<const float4*>(d.g + en));
+        const float4 na4 = __ldg(reinterpret_cast<const float4*>(d.m[0] + en));
+        const float4 nb4 = __ldg(reinterpret_cast<const float4*>(d.m[1] + en));
+        const float4 nc4 = __ldg(reinterpret_cast<const float4*>(d.m[2] + en));
+        const float4 nv4 = __ldg(reinterpret_cast<const float4*>(d.v + en));
         const float4 k0 = __ldg(reinterpret_cast<const float4*>(d.c[0] + w.j));
         const float4 k1 = __ldg(reinterpret_cast<const float4*>(d.c[1] + w.j));
         const float4 k2 = __ldg(reinterpret_cast<const float4*>(d.c[2] + w.j));
@@ -120,6 +130,7 @@ __global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per
           const float c[3] = {c0[q], c1[q], c2[q]};
           lopt_feature_squares(pp[q], gg[q], m, vv[q], r, c, inv_rho, acc);
         }
+        p4 = np4; g4 = ng4; a4 = na4; b4 = nb4; c4 = nc4; v4 = nv4;
       }
     }
   } else {
