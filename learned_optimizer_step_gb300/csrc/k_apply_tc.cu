@@ -205,6 +205,52 @@ __device__ __forceinline__ void pack_relu_row(const uint32_t (&h)[NP], uint32_t 
     av[q] = 2 * q < NP ? relu_f16x2(__uint_as_float(h[2 * q]), __uint_as_float(h[2 * q + 1])) : 0u;
 }
 
+// The accumulator update and the 28 features of one element, normalised by
+// the scales sc and packed as FP16 pairs (feature order as in lopt_features).
+// m and v get exactly lopt_features' arithmetic (they are stored); the
+// features themselves, which go to FP16, use paired FP32 multiplies where two
+// neighbouring features share the operation, and a fused multiply-add
+// inside rsqrt(r c / rho + eps).
+__device__ __forceinline__ void features_f16(float p, float g, float (&m)[3], float& v, const float (&r)[3],
+                                             const float (&c)[3], const float (&inv_rho)[3], const float* sc,
+                                             uint32_t (&av)[16]) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) m[k] = ffma(beta(k), m[k], fmul(one_minus_beta(k), g));
+  v = ffma(kBeta2, v, fmul(kOneMinusBeta2, fmul(g, g)));
+  const float rsv = frsqrt(fadd(v, kEps));
+  float rvh[3], sr[3], sq[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    rvh[k] = frsqrt(fmaf(fmul(r[k], inv_rho[k]), c[k], kEps));
+    sr[k] = fmul(r[k], frsqrt(fadd(r[k], kEps)));
+    sq[k] = fmul(c[k], frsqrt(fadd(c[k], kEps)));
+  }
+  float2 q[14];
+  q[0] = make_float2(p, g);
+  q[1] = make_float2(m[0], m[1]);
+  q[2] = make_float2(m[2], fmul(v, rsv));
+  q[3] = __fmul2_rn(make_float2(m[0], m[1]), make_float2(rsv, rsv));
+  q[4] = __fmul2_rn(make_float2(m[2], g), make_float2(rsv, rsv));
+  q[5] = __fmul2_rn(make_float2(g, g), make_float2(rvh[0], rvh[1]));
+  q[6] = make_float2(fmul(g, rvh[2]), sr[0]);
+  q[7] = make_float2(sr[1], sr[2]);
+  q[8] = make_float2(sq[0], sq[1]);
+  q[9] = make_float2(sq[2], fmul(m[0], rvh[0]));
+  q[10] = __fmul2_rn(make_float2(m[0], m[0]), make_float2(rvh[1], rvh[2]));
+  q[11] = __fmul2_rn(make_float2(m[1], m[1]), make_float2(rvh[0], rvh[1]));
+  q[12] = __fmul2_rn(make_float2(m[1], m[2]), make_float2(rvh[2], rvh[0]));
+  q[13] = __fmul2_rn(make_float2(m[2], m[2]), make_float2(rvh[1], rvh[2]));
+  const float4* sc4 = reinterpret_cast<const float4*>(sc);
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    const float4 s = sc4[k];
+    const float2 lo = __fmul2_rn(q[2 * k], make_float2(s.x, s.y));
+    const float2 hi = __fmul2_rn(q[2 * k + 1], make_float2(s.z, s.w));
+    av[2 * k] = f16x2(lo.x, lo.y);
+    av[2 * k + 1] = f16x2(hi.x, hi.y);
+  }
+}
+
 template <int NP>
 __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, uint32_t (&r)[NP]) {
   if constexpr (NP == 16) tmem_ld16(taddr, r);
@@ -462,9 +508,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             float inv_rho[3];
 #pragma unroll
             for (int q = 0; q < 3; ++q) inv_rho[q] = rc.inv_rho[q];
-            const RowTerms rt = row_terms_of(r, inv_rho);
-            float f[kStats];
-            lopt_features(p, g, m, v, rt, c, f);
+            // normalised features, FP16, for this lane's row of the slot's A
+            // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
+            uint32_t av[16];
+            features_f16(p, g, m, v, r, c, inv_rho, rc.sc, av);
             if (stg) {
               sbase[2 * kStageElems + x] = m[0]; sbase[3 * kStageElems + x] = m[1];
               sbase[4 * kStageElems + x] = m[2]; sbase[5 * kStageElems + x] = v;
@@ -474,16 +521,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
 #pragma unroll
               for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
               d.v[e] = v;
-            }
-            // normalised features, FP16, into this lane's row of the slot's A
-            // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
-            uint32_t av[16];
-            const float4* sc4 = reinterpret_cast<const float4*>(rc.sc);
-#pragma unroll
-            for (int q = 0; q < 7; ++q) {
-              const float4 sq = sc4[q];
-              av[2 * q] = f16x2(f[4 * q] * sq.x, f[4 * q + 1] * sq.y);
-              av[2 * q + 1] = f16x2(f[4 * q + 2] * sq.z, f[4 * q + 3] * sq.w);
             }
             av[14] = 0x00003C00u;   // 1.0h, 0
             av[15] = 0u;
