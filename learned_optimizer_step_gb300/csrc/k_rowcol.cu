@@ -116,6 +116,7 @@ __device__ void strip_pass(const TensorDesc& d, int64_t r0, int nrows, float* co
 // of its columns in registers until the warps' column sums are combined in
 // warp order.  Same results in every run: every sum has a fixed order.
 constexpr int kColVec = 4;                 // vectors of W columns per lane and segment
+constexpr int kRowUnroll = 2;              // rows whose loads a warp has in flight together
 
 template <int W>
 __device__ void strip_rows_pass(const TensorDesc& d, int64_t r0, int nrows, float* colpart_strip,
@@ -131,46 +132,57 @@ __device__ void strip_rows_pass(const TensorDesc& d, int64_t r0, int nrows, floa
     for (int v = 0; v < kColVec; ++v)
 #pragma unroll
       for (int q = 0; q < W; ++q) col[v][q] = 0.f;
-    for (int row = warp; row < nrows; row += kWarps) {
-      const float* src = d.g + (r0 + row) * C + c0;
-      // all loads of the row segment first, so that they are in flight
-      // together: a column past the end reads the segment's first column
-      // (in bounds) and counts as zero
-      float x[kColVec][W];
+    for (int row0 = warp; row0 < nrows; row0 += kRowUnroll * kWarps) {
+      // all loads of kRowUnroll row segments first, so that they are in
+      // flight together: a row past the strip reads row0 again and a column
+      // past the end the segment's first column (both in bounds); neither
+      // is counted
+      float x[kRowUnroll][kColVec][W];
 #pragma unroll
-      for (int v = 0; v < kColVec; ++v) {
-        const int64_t j = (int64_t)(v * 32 + lane) * W;   // column offset in the segment
-        const int64_t js = c0 + j < C ? j : 0;
-        if constexpr (W == 4) {
-          const float4 y = __ldg(reinterpret_cast<const float4*>(src + js));
-          x[v][0] = y.x; x[v][1] = y.y; x[v][2] = y.z; x[v][3] = y.w;
-        } else {
-          x[v][0] = __ldg(src + js);
-        }
-      }
-      float rs = 0.f;
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int row = row0 + u * kWarps < nrows ? row0 + u * kWarps : row0;
+        const float* src = d.g + (r0 + row) * C + c0;
 #pragma unroll
-      for (int v = 0; v < kColVec; ++v) {
-        const int64_t j = (int64_t)(v * 32 + lane) * W;
-        if (c0 + j < C) {
+        for (int v = 0; v < kColVec; ++v) {
+          const int64_t j = (int64_t)(v * 32 + lane) * W;   // column offset in the segment
+          const int64_t js = c0 + j < C ? j : 0;
           if constexpr (W == 4) {
-            const float s0 = fmul(x[v][0], x[v][0]), s1 = fmul(x[v][1], x[v][1]);
-            const float s2 = fmul(x[v][2], x[v][2]), s3 = fmul(x[v][3], x[v][3]);
-            col[v][0] = fadd(col[v][0], s0);
-            col[v][1] = fadd(col[v][1], s1);
-            col[v][2] = fadd(col[v][2], s2);
-            col[v][3] = fadd(col[v][3], s3);
-            rs = fadd(rs, fadd(fadd(s0, s1), fadd(s2, s3)));
+            const float4 y = __ldg(reinterpret_cast<const float4*>(src + js));
+            x[u][v][0] = y.x; x[u][v][1] = y.y; x[u][v][2] = y.z; x[u][v][3] = y.w;
           } else {
-            const float s0 = fmul(x[v][0], x[v][0]);
-            col[v][0] = fadd(col[v][0], s0);
-            rs = fadd(rs, s0);
+            x[u][v][0] = __ldg(src + js);
           }
         }
       }
+      // rows in increasing order, as one row at a time would add them
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) rs = fadd(rs, __shfl_xor_sync(0xffffffffu, rs, off));
-      if (lane == 0) rowacc[row] = fadd(rowacc[row], rs);
+      for (int u = 0; u < kRowUnroll; ++u) {
+        const int row = row0 + u * kWarps;
+        if (row >= nrows) break;
+        float rs = 0.f;
+#pragma unroll
+        for (int v = 0; v < kColVec; ++v) {
+          const int64_t j = (int64_t)(v * 32 + lane) * W;
+          if (c0 + j < C) {
+            if constexpr (W == 4) {
+              const float s0 = fmul(x[u][v][0], x[u][v][0]), s1 = fmul(x[u][v][1], x[u][v][1]);
+              const float s2 = fmul(x[u][v][2], x[u][v][2]), s3 = fmul(x[u][v][3], x[u][v][3]);
+              col[v][0] = fadd(col[v][0], s0);
+              col[v][1] = fadd(col[v][1], s1);
+              col[v][2] = fadd(col[v][2], s2);
+              col[v][3] = fadd(col[v][3], s3);
+              rs = fadd(rs, fadd(fadd(s0, s1), fadd(s2, s3)));
+            } else {
+              const float s0 = fmul(x[u][v][0], x[u][v][0]);
+              col[v][0] = fadd(col[v][0], s0);
+              rs = fadd(rs, s0);
+            }
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) rs = fadd(rs, __shfl_xor_sync(0xffffffffu, rs, off));
+        if (lane == 0) rowacc[row] = fadd(rowacc[row], rs);
+      }
     }
     // this warp's column sums, then the warps' sums in warp order
 #pragma unroll

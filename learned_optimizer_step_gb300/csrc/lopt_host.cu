@@ -192,6 +192,14 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
     for (int s = 0; s < d.k2_units; ++s) units[2].push_back({i, s});
   }
   h->w1fold_stride = w1fold_floats(h->hp, h->path);
+  // K0 blocks are dispatched about in unit order: the largest strips first
+  // (whose tensors also have the longest column finalisation), so that the
+  // launch ends on small strips.  Results do not depend on this order.
+  std::stable_sort(units[0].begin(), units[0].end(), [&](const Unit& x, const Unit& y) {
+    const TensorDesc& a = desc[x.tensor];
+    const TensorDesc& b = desc[y.tensor];
+    return (int64_t)a.strip_rows * a.C > (int64_t)b.strip_rows * b.C;
+  });
 
   // carve the workspace
   size_t off = 0;
