@@ -161,6 +161,37 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
               int64_t t, float lr, void* stream);
 
 /*
+ * The same step for a training loop that holds gradients and parameters in
+ * HOST memory: for each tensor i, grad_host[i] (rows * cols floats) is copied
+ * into tensors[i].grad before tensor i is stepped, and the updated
+ * tensors[i].param is copied into param_host[i] (rows * cols floats) after
+ * it.  The accumulators (mom, rms, row, col) and the device copies of param
+ * and grad stay on the device and are updated as by lopt_step().
+ *
+ * Per tensor the step is the same computation as lopt_step() (every
+ * normalisation statistic belongs to one tensor), so results are
+ * identical.  The list is cut into up to 8 groups of consecutive tensors of
+ * about equal size (at least 4 Mi elements each), each stepped by its own
+ * three launches; the copies run on two streams of the handle, so that the
+ * gradient copies of group k+1 and the parameter copies of group k-1 overlap
+ * the kernels of group k.
+ *
+ * grad_host, param_host: HOST arrays of n_tensors HOST pointers, read during
+ * the call only.  The buffers must not overlap one another; page-locked
+ * memory (cudaHostAlloc, or pinned) lets the copies overlap the kernels,
+ * pageable memory works without that.  Asynchronous on `stream` like
+ * lopt_step(): once the work this call enqueued on `stream` has completed,
+ * param_host[i] holds the new parameters and grad_host[i] may be reused.
+ * Kernel timing (lopt_set_kernel_timing) and lopt_feature_stats() cover
+ * lopt_step() calls only.
+ * Errors: as lopt_step(); LOPT_E_ARG also for a NULL host pointer of a
+ * non-empty tensor and during a row-sharded step.
+ */
+int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
+                   const float* const* grad_host, float* const* param_host,
+                   int64_t t, float lr, void* stream);
+
+/*
  * ---- Row-sharded step (data parallel over ranks) --------------------------
  * The step of the PyLO pages' distributed optimiser (section "分散最適化
  * ステップ": each rank owns a slice of the optimiser state, as after a

@@ -40,6 +40,8 @@ int strip_rows_for(int64_t R, int64_t C) {
 
 using namespace lopt;
 
+struct HostPipe;
+
 struct lopt_ctx {
   int device = 0;
   int hidden = 0;        // caller's width
@@ -77,6 +79,10 @@ struct lopt_ctx {
   // ordering across calls
   cudaEvent_t done = nullptr;
   bool has_done = false;
+  // host-buffer steps: one context per group of tensors, created on first use;
+  // the parts share the parent's weights
+  HostPipe* pipe = nullptr;
+  bool shared_weights = false;
   // optional per-kernel timing: 4 events per timed step
   bool timing = false;
   std::vector<cudaEvent_t> tev;
@@ -313,6 +319,62 @@ int leave_phase(lopt_ctx* h, cudaStream_t stream, cudaError_t e) {
 
 }  // namespace
 
+// ---- host-buffer steps ------------------------------------------------------
+constexpr int kHostGroups = 8;                 // most groups of tensors per step
+constexpr int64_t kHostGroupElems = 1 << 22;   // fewest elements per group
+
+struct HostPipe {
+  std::vector<lopt_ctx*> parts;    // one context per group (weights shared with the parent)
+  std::vector<int> split;          // group g: tensors [split[g], split[g + 1])
+  std::vector<lopt_tensor> list;   // the list the split was made for
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> ev;     // per group: gradients in, step enqueued, parameters out
+  cudaEvent_t entry = nullptr;
+};
+
+namespace {
+
+// Consecutive groups of about equal element counts: up to kHostGroups, at
+// least kHostGroupElems elements each (one group for a small list), at
+// least one tensor each.
+void split_groups(const lopt_tensor* ts, int n, std::vector<int>& split) {
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) total += ts[i].rows * ts[i].cols;
+  int G = (int)std::min<int64_t>(kHostGroups, std::max<int64_t>(1, total / kHostGroupElems));
+  G = std::min(G, n);
+  split.assign(1, 0);
+  int64_t acc = 0;
+  for (int i = 0; i + 1 < n; ++i) {
+    acc += ts[i].rows * ts[i].cols;
+    const int g = (int)split.size();   // the boundary that closes group g - 1
+    if (g < G && acc * G >= total * g && n - (i + 1) >= G - g) split.push_back(i + 1);
+  }
+  split.push_back(n);
+}
+
+// A context for one group: the parent's weights, its own workspace.
+lopt_ctx* make_part(const lopt_ctx* h) {
+  lopt_ctx* c = new (std::nothrow) lopt_ctx();
+  if (!c) return nullptr;
+  c->device = h->device;
+  c->hidden = h->hidden;
+  c->hp = h->hp;
+  c->n_sets = h->n_sets;
+  c->d_weights = h->d_weights;
+  c->d_tcw = h->d_tcw;
+  c->shared_weights = true;
+  if (cudaEventCreateWithFlags(&c->done, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return nullptr;
+  }
+  return c;
+}
+
+void destroy_pipe(HostPipe* p);
+
+}  // namespace
+
 extern "C" {
 
 int lopt_version(void) { return 100; }
@@ -516,6 +578,108 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   return LOPT_OK;
 }
 
+int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors, const float* const* grad_host,
+                   float* const* param_host, int64_t t, float lr, void* stream_ptr) {
+  if (!h || n_tensors < 0 || (n_tensors > 0 && (!tensors || !grad_host || !param_host))) return LOPT_E_ARG;
+  if (t < 1 || h->shard_phase != 0 || h->shared_weights) return LOPT_E_ARG;
+  for (int i = 0; i < n_tensors; ++i)
+    if (tensors[i].rows * tensors[i].cols > 0 && (!grad_host[i] || !param_host[i])) return LOPT_E_ARG;
+  if (n_tensors == 0) return LOPT_OK;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
+
+  HostPipe* p = h->pipe;
+  const bool same = p && (int)p->list.size() == n_tensors &&
+                    std::memcmp(p->list.data(), tensors, sizeof(lopt_tensor) * n_tensors) == 0;
+  if (!same) {   // nothing is enqueued before the whole list has passed
+    const int rc = validate(h, tensors, n_tensors);
+    if (rc != LOPT_OK) return rc;
+  }
+  PhaseScope sc;
+  int rc = enter_phase(h, stream, sc);
+  if (rc != LOPT_OK) return rc;
+  cudaError_t e = cudaSuccess;
+  if (!p) {
+    p = h->pipe = new (std::nothrow) HostPipe();
+    if (!p) return LOPT_E_OOM;
+    e = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->entry, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      destroy_pipe(p);
+      h->pipe = nullptr;
+      return cuda_fail(e);
+    }
+  }
+  if (!same) {
+    p->list.clear();
+    split_groups(tensors, n_tensors, p->split);
+    const int G = (int)p->split.size() - 1;
+    while ((int)p->parts.size() < G) {
+      lopt_ctx* c = make_part(h);
+      if (!c) return LOPT_E_OOM;
+      p->parts.push_back(c);
+    }
+    while ((int)p->ev.size() < 3 * G) {
+      cudaEvent_t x;
+      if ((e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+      p->ev.push_back(x);
+    }
+    p->list.assign(tensors, tensors + n_tensors);
+  }
+  const int G = (int)p->split.size() - 1;
+  // One copy per run of tensors that follow each other without a gap on
+  // both sides (as in flat parameter buffers), else one per tensor.
+  auto copy_runs = [&](int i0, int i1, auto dst_of, auto src_of, cudaMemcpyKind kind, cudaStream_t st) {
+    cudaError_t err = cudaSuccess;
+    float* dst = nullptr;
+    const float* src = nullptr;
+    size_t n = 0;
+    for (int i = i0; i <= i1 && err == cudaSuccess; ++i) {
+      const size_t k = i < i1 ? (size_t)(tensors[i].rows * tensors[i].cols) : 0;
+      if (i < i1 && k == 0) continue;
+      if (i < i1 && n && dst_of(i) == dst + n && src_of(i) == src + n) {
+        n += k;
+        continue;
+      }
+      if (n) err = cudaMemcpyAsync(dst, src, n * sizeof(float), kind, st);
+      if (i < i1) {
+        dst = dst_of(i);
+        src = src_of(i);
+        n = k;
+      }
+    }
+    return err;
+  };
+
+  // the copies start after everything enqueued on the stream before this call
+  e = cudaEventRecord(p->entry, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->h2d, p->entry, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->d2h, p->entry, 0);
+  for (int g = 0; g < G && e == cudaSuccess; ++g) {
+    const int i0 = p->split[g], i1 = p->split[g + 1];
+    cudaEvent_t* ev = p->ev.data() + 3 * g;
+    e = copy_runs(i0, i1, [&](int i) { return const_cast<float*>(tensors[i].grad); },
+                  [&](int i) { return const_cast<float*>(grad_host[i]); }, cudaMemcpyHostToDevice, p->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[0], p->h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[0], 0);
+    if (e != cudaSuccess) break;
+    lopt_ctx* c = p->parts[g];
+    c->path = h->path;
+    c->weight_decay = h->weight_decay;
+    rc = lopt_step(c, tensors + i0, i1 - i0, t, lr, stream);
+    if (rc != LOPT_OK) return rc;
+    e = cudaEventRecord(ev[1], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->d2h, ev[1], 0);
+    if (e == cudaSuccess)
+      e = copy_runs(i0, i1, [&](int i) { return param_host[i]; }, [&](int i) { return tensors[i].param; },
+                    cudaMemcpyDeviceToHost, p->d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[2], p->d2h);
+  }
+  // the call is complete on the stream once the last parameters are out
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, p->ev[3 * (G - 1) + 2], 0);
+  return leave_phase(h, stream, e);
+}
+
 int lopt_shard_sizes(const lopt_tensor* tensors, int n_tensors, int64_t* n_x1, int64_t* n_x2) {
   if (n_tensors < 0 || (n_tensors > 0 && !tensors) || !n_x1 || !n_x2) return LOPT_E_ARG;
   shard_counts(tensors, n_tensors, n_x1, n_x2);
@@ -619,6 +783,12 @@ int lopt_shard_end(lopt_handle h, void* stream_ptr) {
 
 int lopt_check(lopt_handle h) {
   if (!h) return LOPT_E_ARG;
+  if (h->pipe) {
+    for (lopt_ctx* c : h->pipe->parts) {
+      const int rc = lopt_check(c);
+      if (rc != LOPT_OK) return rc;
+    }
+  }
   if (!h->has_done) return LOPT_OK;
   cudaError_t e = cudaEventSynchronize(h->done);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -677,13 +847,26 @@ int lopt_kernel_times(lopt_handle h, double* ms, int64_t* launches) {
 int lopt_destroy(lopt_handle h) {
   if (!h) return LOPT_E_ARG;
   if (h->has_done) cudaEventSynchronize(h->done);
+  destroy_pipe(h->pipe);
   for (cudaEvent_t x : h->tev) cudaEventDestroy(x);
   if (h->d_ws) cudaFree(h->d_ws);
-  if (h->d_weights) cudaFree(h->d_weights);
-  if (h->d_tcw) cudaFree(h->d_tcw);
+  if (!h->shared_weights && h->d_weights) cudaFree(h->d_weights);
+  if (!h->shared_weights && h->d_tcw) cudaFree(h->d_tcw);
   if (h->done) cudaEventDestroy(h->done);
   delete h;
   return LOPT_OK;
 }
 
 }  // extern "C"
+
+namespace {
+void destroy_pipe(HostPipe* p) {
+  if (!p) return;
+  for (lopt_ctx* c : p->parts) lopt_destroy(c);
+  for (cudaEvent_t x : p->ev) cudaEventDestroy(x);
+  if (p->entry) cudaEventDestroy(p->entry);
+  if (p->h2d) cudaStreamDestroy(p->h2d);
+  if (p->d2h) cudaStreamDestroy(p->d2h);
+  delete p;
+}
+}  // namespace

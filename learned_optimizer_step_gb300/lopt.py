@@ -32,6 +32,7 @@ ERRORS = {
 }
 
 EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_set_weight_decay", "lopt_step",
+            "lopt_step_host",
             "lopt_shard_sizes", "lopt_shard_begin", "lopt_shard_middle", "lopt_shard_end",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
             "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_version")
@@ -76,6 +77,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_set_weight_decay.argtypes = [vp, ctypes.c_float]
     lib.lopt_set_weight_decay.restype = i32
     lib.lopt_step.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, i64, ctypes.c_float, vp]
+    lib.lopt_step_host.restype = i32
+    lib.lopt_step_host.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                   i64, ctypes.c_float, vp]
     lib.lopt_step.restype = i32
     lib.lopt_shard_sizes.argtypes = [ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.lopt_shard_sizes.restype = i32
@@ -117,6 +121,24 @@ def _ptr(t, n: int, what: str) -> int:
         raise TypeError("%s must be a torch.Tensor" % what)
     if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
         raise TypeError("%s must be a contiguous CUDA float32 tensor" % what)
+    if t.numel() != n:
+        raise ValueError("%s has %d elements, expected %d" % (what, t.numel(), n))
+    return t.data_ptr()
+
+
+def _host_ptr(t, n: int, what: str) -> int:
+    """Address of a CPU float32 buffer of n elements (torch tensor or numpy array)."""
+    import torch
+    if isinstance(t, np.ndarray):
+        if t.dtype != np.float32 or not t.flags["C_CONTIGUOUS"] or not t.flags["WRITEABLE"]:
+            raise TypeError("%s must be a writeable contiguous float32 array" % what)
+        if t.size != n:
+            raise ValueError("%s has %d elements, expected %d" % (what, t.size, n))
+        return t.ctypes.data
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor or a numpy array" % what)
+    if t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous CPU float32 tensor" % what)
     if t.numel() != n:
         raise ValueError("%s has %d elements, expected %d" % (what, t.numel(), n))
     return t.data_ptr()
@@ -212,6 +234,24 @@ class LearnedOptimizer:
         handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
         _check("lopt_step", load_library().lopt_step(self._h, pl.array, pl.n, int(t), float(lr),
                                                       ctypes.c_void_p(handle)))
+
+    def step_host(self, tensors, grad_host, param_host, t: int, lr: float = 1.0,
+                  stream: Optional[object] = None) -> None:
+        """One step with gradients coming from and parameters going to host
+        memory: grad_host[i] is copied into tensor i's device gradient before
+        its step and the new parameters into param_host[i] after it (CPU
+        float32 buffers of rows * cols elements; pinned memory lets the
+        copies overlap the kernels).  Asynchronous on ``stream``; the host
+        buffers are complete once the stream has passed this call."""
+        pl = tensors if isinstance(tensors, PreparedList) else self.prepare(tensors)
+        if len(grad_host) != pl.n or len(param_host) != pl.n:
+            raise ValueError("one host gradient and one host parameter buffer per tensor")
+        gp = (ctypes.c_void_p * pl.n)(*[_host_ptr(x, ts.rows * ts.cols, "grad_host[%d]" % i)
+                                        for i, (x, ts) in enumerate(zip(grad_host, pl.tensors))])
+        pp = (ctypes.c_void_p * pl.n)(*[_host_ptr(x, ts.rows * ts.cols, "param_host[%d]" % i)
+                                        for i, (x, ts) in enumerate(zip(param_host, pl.tensors))])
+        _check("lopt_step_host", load_library().lopt_step_host(self._h, pl.array, pl.n, gp, pp, int(t), float(lr),
+                                                                self._stream(stream)))
 
     # ---- row-sharded step --------------------------------------------------
     @staticmethod

@@ -6,6 +6,8 @@ import ctypes
 import os
 import re
 
+import numpy as np
+
 import pytest
 
 from learned_optimizer_step_gb300 import build as B
@@ -70,6 +72,7 @@ def test_validation_before_any_device_call(lib):
     assert lib.lopt_create(fp, 39, 65, 1, ctypes.byref(h)) == -6
     assert h.value is None
     assert lib.lopt_step(None, None, 0, 1, 1.0, None) == -1
+    assert lib.lopt_step_host(None, None, 0, None, None, 1, 1.0, None) == -1
     assert lib.lopt_check(None) == -1
     assert lib.lopt_destroy(None) == -1
     assert lib.lopt_set_mlp_path(None, 0) == -1
@@ -85,3 +88,15 @@ def test_binding_rejects_non_cuda_tensors():
     t = torch.zeros(4)
     with pytest.raises(TypeError):
         L._ptr(t, 4, "param")
+
+
+def test_binding_host_buffers_must_be_cpu_float32():
+    torch = pytest.importorskip("torch")
+    assert L._host_ptr(torch.zeros(4), 4, "g") != 0
+    assert L._host_ptr(np.zeros(4, np.float32), 4, "g") != 0
+    with pytest.raises(TypeError):
+        L._host_ptr(torch.zeros(4, dtype=torch.float64), 4, "g")
+    with pytest.raises(TypeError):
+        L._host_ptr(np.zeros(4), 4, "g")
+    with pytest.raises(ValueError):
+        L._host_ptr(torch.zeros(5), 4, "g")
