@@ -234,11 +234,11 @@ def flat_states(wl, device, seed=0):
 
 
 def kernel_source_sha(path: str) -> str:
+    """Hash of a kernel's source and the headers it includes."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "learned_optimizer_step_gb300", "csrc", path), "rb") as fh:
-        h.update(fh.read())
-    with open(os.path.join(ROOT, "learned_optimizer_step_gb300", "csrc", "lopt_internal.cuh"), "rb") as fh:
-        h.update(fh.read())
+    for name in (path, "lopt_internal.cuh", "tc_layout.cuh"):
+        with open(os.path.join(ROOT, "learned_optimizer_step_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
