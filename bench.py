@@ -353,7 +353,7 @@ def run_ours(args, rank, world, local_rank):
     # ---- end to end through the public API with host buffers ----
     # every step copies each tensor's gradient in from pinned host memory and
     # its new parameters out (lopt_step_host: groups of tensors pipelined
-    # with their copies on two more streams)
+    # with their copies on two more streams, also across steps)
     h_g = torch.empty(nflat, dtype=torch.float32, pin_memory=True)
     h_g.copy_(flat["grad"])
     h_p = torch.empty(nflat, dtype=torch.float32, pin_memory=True)
@@ -369,6 +369,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(e2e_steps):
         eng.step_host(prepared, g_host, p_host, t, 1.0, stream)
         t += 1
+    eng.host_sync(stream)   # the last parameters are in host memory
     e1.record(stream)
     barrier()
     eng.check()

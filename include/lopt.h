@@ -162,34 +162,54 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
 
 /*
  * The same step for a training loop that holds gradients and parameters in
- * HOST memory: for each tensor i, grad_host[i] (rows * cols floats) is copied
- * into tensors[i].grad before tensor i is stepped, and the updated
- * tensors[i].param is copied into param_host[i] (rows * cols floats) after
- * it.  The accumulators (mom, rms, row, col) and the device copies of param
- * and grad stay on the device and are updated as by lopt_step().
+ * HOST memory: for each tensor i, grad_host[i] (rows * cols floats) is the
+ * gradient, and the updated parameters are copied into param_host[i]
+ * (rows * cols floats).  tensors[i].grad is not used (it may be NULL): the
+ * gradients go through two device staging buffers of the handle, used by
+ * alternate calls.  The accumulators (mom, rms, row, col) and the device
+ * parameters are updated as by lopt_step().
  *
  * Per tensor the step is the same computation as lopt_step() (every
  * normalisation statistic belongs to one tensor), so results are
  * identical.  The list is cut into up to 8 groups of consecutive tensors of
  * about equal size (at least 4 Mi elements each), each stepped by its own
- * three launches; the copies run on two streams of the handle, so that the
- * gradient copies of group k+1 and the parameter copies of group k-1 overlap
- * the kernels of group k.
+ * three launches on `stream`; the copies run on two streams of the handle,
+ * so that gradient and parameter copies overlap the kernels of other
+ * groups, also across consecutive calls.  Adjacent tensors whose buffers
+ * follow each other on both sides move in one copy.
+ *
+ * Ordering.  The kernels are ordered with other work on `stream`.  The
+ * parameter copies are not: they may still run after `stream` has passed
+ * the call.  Before reading param_host, writing new gradients into the
+ * same grad_host buffers, or touching the device parameters with other
+ * work, call lopt_host_sync() on the stream that does so (or lopt_check(),
+ * which waits on the host).  lopt_step() and the sharded calls of the
+ * handle wait for these copies by themselves.
  *
  * grad_host, param_host: HOST arrays of n_tensors HOST pointers, read during
  * the call only.  The buffers must not overlap one another; page-locked
  * memory (cudaHostAlloc, or pinned) lets the copies overlap the kernels,
- * pageable memory works without that.  Asynchronous on `stream` like
- * lopt_step(): once the work this call enqueued on `stream` has completed,
- * param_host[i] holds the new parameters and grad_host[i] may be reused.
- * Kernel timing (lopt_set_kernel_timing) and lopt_feature_stats() cover
- * lopt_step() calls only.
- * Errors: as lopt_step(); LOPT_E_ARG also for a NULL host pointer of a
- * non-empty tensor and during a row-sharded step.
+ * pageable memory works without that.  The staging buffers take 2 x 4 bytes
+ * per element of device memory, allocated on the first call with a new
+ * list.  Kernel timing (lopt_set_kernel_timing) and lopt_feature_stats()
+ * cover lopt_step() calls only.
+ * Errors: as lopt_step() (validation covers the list with its staging
+ * gradients); LOPT_E_ARG also for a NULL host pointer of a non-empty tensor
+ * and during a row-sharded step; LOPT_E_OOM if the staging buffers cannot
+ * be allocated.
  */
 int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
                    const float* const* grad_host, float* const* param_host,
                    int64_t t, float lr, void* stream);
+
+/*
+ * Makes `stream` wait (without blocking the host) until every parameter
+ * copy of the handle's host-buffer steps enqueued so far is done: after it,
+ * work on `stream` may read param_host, and the host may use param_host and
+ * refill grad_host once `stream` has reached this point.
+ * Errors: LOPT_E_ARG (NULL handle), LOPT_E_CUDA.
+ */
+int lopt_host_sync(lopt_handle h, void* stream);
 
 /*
  * ---- Row-sharded step (data parallel over ranks) --------------------------
@@ -300,6 +320,14 @@ int lopt_destroy(lopt_handle h);
 
 /* Static string naming an error code. */
 const char* lopt_strerror(int code);
+
+/*
+ * Name and description of the last CUDA error on which a call made by this
+ * host thread returned LOPT_E_CUDA or LOPT_E_OOM ("" if none yet).  The
+ * string belongs to the library and stays valid until the thread's next
+ * failing call.
+ */
+const char* lopt_last_cuda_error(void);
 
 /* Library version as major*10000 + minor*100 + patch. */
 int lopt_version(void);

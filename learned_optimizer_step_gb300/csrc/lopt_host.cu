@@ -10,6 +10,7 @@
 // "メモリ階層の活用") counts 30-114 launches per step for a whole model with
 // its two fused kernels per tensor; here the whole list takes three.
 #include <algorithm>
+#include <string>
 #include <cmath>
 #include <cstddef>
 #include <cstdio>
@@ -91,7 +92,11 @@ struct lopt_ctx {
 
 namespace {
 
+// The last CUDA error a call of this thread failed on (lopt_last_cuda_error).
+thread_local std::string g_last_cuda;
+
 int cuda_fail(cudaError_t e) {
+  g_last_cuda = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
   if (e == cudaErrorMemoryAllocation) return LOPT_E_OOM;
   return LOPT_E_CUDA;
 }
@@ -323,14 +328,24 @@ int leave_phase(lopt_ctx* h, cudaStream_t stream, cudaError_t e) {
 constexpr int kHostGroups = 8;                 // most groups of tensors per step
 constexpr int64_t kHostGroupElems = 1 << 22;   // fewest elements per group
 
+// Consecutive calls alternate between two device staging buffers for the
+// gradients, so that the gradient copies of one call can run while the
+// kernels of the previous call still read the other buffer.
 struct HostPipe {
-  std::vector<lopt_ctx*> parts;    // one context per group (weights shared with the parent)
-  std::vector<int> split;          // group g: tensors [split[g], split[g + 1])
-  std::vector<lopt_tensor> list;   // the list the split was made for
+  std::vector<lopt_ctx*> parts[2];      // per staging buffer, one context per group
+  std::vector<int> split;               // group g: tensors [split[g], split[g + 1])
+  std::vector<lopt_tensor> list;        // the caller's list the set-up was made for
+  std::vector<lopt_tensor> staged[2];   // the same list reading its gradients from buffer q
+  float* stage[2] = {nullptr, nullptr};
+  size_t stage_floats = 0;
+  int q = 0;                            // staging buffer of the next call
+  bool any = false;                     // a host-buffer step has been enqueued
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  std::vector<cudaEvent_t> ev;     // per group: gradients in, step enqueued, parameters out
-  cudaEvent_t entry = nullptr;
+  // per group: gradients in (per buffer), kernels done (per buffer), parameters out
+  std::vector<cudaEvent_t> ev;
+  cudaEvent_t d2h_done = nullptr;       // after the last parameter copy issued
 };
+constexpr int kGroupEvents = 5;
 
 namespace {
 
@@ -373,11 +388,20 @@ lopt_ctx* make_part(const lopt_ctx* h) {
 
 void destroy_pipe(HostPipe* p);
 
+// Work that reads or writes the device parameters waits for the host-buffer
+// steps' parameter copies still in flight.
+cudaError_t wait_host_copies(const lopt_ctx* h, cudaStream_t stream) {
+  if (!h->pipe || !h->pipe->any) return cudaSuccess;
+  return cudaStreamWaitEvent(stream, h->pipe->d2h_done, 0);
+}
+
 }  // namespace
 
 extern "C" {
 
 int lopt_version(void) { return 100; }
+
+const char* lopt_last_cuda_error(void) { return g_last_cuda.c_str(); }
 
 const char* lopt_strerror(int code) {
   switch (code) {
@@ -503,6 +527,8 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
     e = cudaStreamWaitEvent(stream, h->done, 0);
     if (e != cudaSuccess) return cuda_fail(e);
   }
+  e = wait_host_copies(h, stream);
+  if (e != cudaSuccess) return cuda_fail(e);
   if (!same) {
     int rc = build_schedule(h, tensors, n_tensors, stream);
     if (rc != LOPT_OK) {
@@ -587,53 +613,101 @@ int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors, con
   if (n_tensors == 0) return LOPT_OK;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
 
-  HostPipe* p = h->pipe;
-  const bool same = p && (int)p->list.size() == n_tensors &&
-                    std::memcmp(p->list.data(), tensors, sizeof(lopt_tensor) * n_tensors) == 0;
-  if (!same) {   // nothing is enqueued before the whole list has passed
-    const int rc = validate(h, tensors, n_tensors);
-    if (rc != LOPT_OK) return rc;
-  }
   PhaseScope sc;
   int rc = enter_phase(h, stream, sc);
   if (rc != LOPT_OK) return rc;
   cudaError_t e = cudaSuccess;
+  HostPipe* p = h->pipe;
   if (!p) {
     p = h->pipe = new (std::nothrow) HostPipe();
     if (!p) return LOPT_E_OOM;
     e = cudaStreamCreateWithFlags(&p->h2d, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&p->d2h, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->entry, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->d2h_done, cudaEventDisableTiming);
     if (e != cudaSuccess) {
       destroy_pipe(p);
       h->pipe = nullptr;
       return cuda_fail(e);
     }
   }
+  const bool same = (int)p->list.size() == n_tensors &&
+                    std::memcmp(p->list.data(), tensors, sizeof(lopt_tensor) * n_tensors) == 0;
   if (!same) {
+    // a new list: earlier host-buffer steps must be done with the buffers
     p->list.clear();
+    if (p->any && (e = cudaEventSynchronize(p->d2h_done)) != cudaSuccess) return cuda_fail(e);
+    if (h->has_done && (e = cudaEventSynchronize(h->done)) != cudaSuccess) return cuda_fail(e);
+    std::vector<size_t> off((size_t)n_tensors);
+    size_t need = 0;
+    for (int i = 0; i < n_tensors; ++i) {
+      off[i] = need;
+      need += ((size_t)(tensors[i].rows * tensors[i].cols) + 3) / 4 * 4;   // 16-byte aligned starts
+    }
+    need = std::max<size_t>(need, 4);
+    if (need > p->stage_floats) {
+      for (int q = 0; q < 2; ++q) {
+        if (p->stage[q]) cudaFree(p->stage[q]);
+        p->stage[q] = nullptr;
+      }
+      p->stage_floats = 0;
+      for (int q = 0; q < 2; ++q) {
+        if ((e = cudaMalloc(&p->stage[q], need * sizeof(float))) != cudaSuccess) {
+          cudaGetLastError();
+          return LOPT_E_OOM;
+        }
+      }
+      p->stage_floats = need;
+    }
+    for (int q = 0; q < 2; ++q) {
+      p->staged[q].assign(tensors, tensors + n_tensors);
+      for (int i = 0; i < n_tensors; ++i) p->staged[q][i].grad = p->stage[q] + off[i];
+      if ((rc = validate(h, p->staged[q].data(), n_tensors)) != LOPT_OK) return rc;
+    }
     split_groups(tensors, n_tensors, p->split);
     const int G = (int)p->split.size() - 1;
-    while ((int)p->parts.size() < G) {
-      lopt_ctx* c = make_part(h);
-      if (!c) return LOPT_E_OOM;
-      p->parts.push_back(c);
+    for (int q = 0; q < 2; ++q) {
+      while ((int)p->parts[q].size() < G) {
+        lopt_ctx* c = make_part(h);
+        if (!c) return LOPT_E_OOM;
+        p->parts[q].push_back(c);
+      }
     }
-    while ((int)p->ev.size() < 3 * G) {
+    while ((int)p->ev.size() < kGroupEvents * G) {
       cudaEvent_t x;
       if ((e = cudaEventCreateWithFlags(&x, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
       p->ev.push_back(x);
+      // recorded once with nothing before it, so that the first waits on it pass
+      if ((e = cudaEventRecord(x, p->h2d)) != cudaSuccess) return cuda_fail(e);
     }
+    p->q = 0;
     p->list.assign(tensors, tensors + n_tensors);
   }
   const int G = (int)p->split.size() - 1;
+  const int q = p->q;
+  const lopt_tensor* const st = p->staged[q].data();
   // One copy per run of tensors that follow each other without a gap on
-  // both sides (as in flat parameter buffers), else one per tensor.
-  auto copy_runs = [&](int i0, int i1, auto dst_of, auto src_of, cudaMemcpyKind kind, cudaStream_t st) {
+  // both sides (as in flat parameter buffers), else one per tensor.  Two
+  // buffers can also touch by chance while being separate allocations; the
+  // runtime refuses a copy across them (invalid value, before anything is
+  // enqueued), and that run then goes tensor by tensor.
+  auto copy_runs = [&](int i0, int i1, auto dst_of, auto src_of, cudaMemcpyKind kind, cudaStream_t cs) {
     cudaError_t err = cudaSuccess;
     float* dst = nullptr;
     const float* src = nullptr;
     size_t n = 0;
+    int r0 = i0;   // first tensor of the run
+    auto flush = [&](int r1) {
+      if (!n) return cudaSuccess;
+      cudaError_t x = cudaMemcpyAsync(dst, src, n * sizeof(float), kind, cs);
+      if (x != cudaErrorInvalidValue || r1 - r0 < 2) return x;
+      cudaGetLastError();
+      x = cudaSuccess;
+      for (int j = r0; j < r1 && x == cudaSuccess; ++j) {
+        const size_t k = (size_t)(tensors[j].rows * tensors[j].cols);
+        if (k) x = cudaMemcpyAsync(dst_of(j), src_of(j), k * sizeof(float), kind, cs);
+      }
+      return x;
+    };
     for (int i = i0; i <= i1 && err == cudaSuccess; ++i) {
       const size_t k = i < i1 ? (size_t)(tensors[i].rows * tensors[i].cols) : 0;
       if (i < i1 && k == 0) continue;
@@ -641,43 +715,60 @@ int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors, con
         n += k;
         continue;
       }
-      if (n) err = cudaMemcpyAsync(dst, src, n * sizeof(float), kind, st);
+      err = flush(i);
       if (i < i1) {
         dst = dst_of(i);
         src = src_of(i);
         n = k;
+        r0 = i;
       }
     }
     return err;
   };
 
-  // the copies start after everything enqueued on the stream before this call
-  e = cudaEventRecord(p->entry, stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->h2d, p->entry, 0);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(p->d2h, p->entry, 0);
   for (int g = 0; g < G && e == cudaSuccess; ++g) {
     const int i0 = p->split[g], i1 = p->split[g + 1];
-    cudaEvent_t* ev = p->ev.data() + 3 * g;
-    e = copy_runs(i0, i1, [&](int i) { return const_cast<float*>(tensors[i].grad); },
-                  [&](int i) { return const_cast<float*>(grad_host[i]); }, cudaMemcpyHostToDevice, p->h2d);
-    if (e == cudaSuccess) e = cudaEventRecord(ev[0], p->h2d);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[0], 0);
+    cudaEvent_t* ev = p->ev.data() + kGroupEvents * g;   // in[0..1], kernels[2..3], out[4]
+    // gradients into staging buffer q once the kernels of the call before the
+    // previous one (the last to read it) are done with this group
+    e = cudaStreamWaitEvent(p->h2d, ev[2 + q], 0);
+    if (e == cudaSuccess)
+      e = copy_runs(i0, i1, [&](int i) { return const_cast<float*>(st[i].grad); },
+                    [&](int i) { return const_cast<float*>(grad_host[i]); }, cudaMemcpyHostToDevice, p->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[0 + q], p->h2d);
+    // the kernels: after the gradients, and after the previous call's
+    // parameter copies of this group (they read what the kernels overwrite)
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[0 + q], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev[4], 0);
     if (e != cudaSuccess) break;
-    lopt_ctx* c = p->parts[g];
+    lopt_ctx* c = p->parts[q][g];
     c->path = h->path;
     c->weight_decay = h->weight_decay;
-    rc = lopt_step(c, tensors + i0, i1 - i0, t, lr, stream);
+    rc = lopt_step(c, st + i0, i1 - i0, t, lr, stream);
     if (rc != LOPT_OK) return rc;
-    e = cudaEventRecord(ev[1], stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->d2h, ev[1], 0);
+    e = cudaEventRecord(ev[2 + q], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(p->d2h, ev[2 + q], 0);
     if (e == cudaSuccess)
       e = copy_runs(i0, i1, [&](int i) { return param_host[i]; }, [&](int i) { return tensors[i].param; },
                     cudaMemcpyDeviceToHost, p->d2h);
-    if (e == cudaSuccess) e = cudaEventRecord(ev[2], p->d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[4], p->d2h);
   }
-  // the call is complete on the stream once the last parameters are out
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, p->ev[3 * (G - 1) + 2], 0);
+  if (e == cudaSuccess) e = cudaEventRecord(p->d2h_done, p->d2h);
+  if (e == cudaSuccess) {
+    p->q ^= 1;
+    p->any = true;
+  }
   return leave_phase(h, stream, e);
+}
+
+int lopt_host_sync(lopt_handle h, void* stream_ptr) {
+  if (!h) return LOPT_E_ARG;
+  if (!h->pipe || !h->pipe->any) return LOPT_OK;
+  PhaseScope sc;
+  int rc = enter_phase(h, reinterpret_cast<cudaStream_t>(stream_ptr), sc);
+  if (rc != LOPT_OK) return rc;
+  const cudaError_t e = cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream_ptr), h->pipe->d2h_done, 0);
+  return e == cudaSuccess ? LOPT_OK : cuda_fail(e);
 }
 
 int lopt_shard_sizes(const lopt_tensor* tensors, int n_tensors, int64_t* n_x1, int64_t* n_x2) {
@@ -703,6 +794,8 @@ int lopt_shard_begin(lopt_handle h, const lopt_tensor* tensors, const int64_t* g
   PhaseScope sc;
   int rc = enter_phase(h, stream, sc);
   if (rc != LOPT_OK) return rc;
+  const cudaError_t ew = wait_host_copies(h, stream);
+  if (ew != cudaSuccess) return cuda_fail(ew);
   if (!same) {
     rc = build_schedule(h, tensors, n_tensors, stream, global_rows);
     if (rc != LOPT_OK) {
@@ -784,9 +877,15 @@ int lopt_shard_end(lopt_handle h, void* stream_ptr) {
 int lopt_check(lopt_handle h) {
   if (!h) return LOPT_E_ARG;
   if (h->pipe) {
-    for (lopt_ctx* c : h->pipe->parts) {
-      const int rc = lopt_check(c);
-      if (rc != LOPT_OK) return rc;
+    if (h->pipe->any) {
+      const cudaError_t e = cudaEventSynchronize(h->pipe->d2h_done);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    for (int q = 0; q < 2; ++q) {
+      for (lopt_ctx* c : h->pipe->parts[q]) {
+        const int rc = lopt_check(c);
+        if (rc != LOPT_OK) return rc;
+      }
     }
   }
   if (!h->has_done) return LOPT_OK;
@@ -862,9 +961,13 @@ int lopt_destroy(lopt_handle h) {
 namespace {
 void destroy_pipe(HostPipe* p) {
   if (!p) return;
-  for (lopt_ctx* c : p->parts) lopt_destroy(c);
+  if (p->any) cudaEventSynchronize(p->d2h_done);
+  for (int q = 0; q < 2; ++q) {
+    for (lopt_ctx* c : p->parts[q]) lopt_destroy(c);
+    if (p->stage[q]) cudaFree(p->stage[q]);
+  }
   for (cudaEvent_t x : p->ev) cudaEventDestroy(x);
-  if (p->entry) cudaEventDestroy(p->entry);
+  if (p->d2h_done) cudaEventDestroy(p->d2h_done);
   if (p->h2d) cudaStreamDestroy(p->h2d);
   if (p->d2h) cudaStreamDestroy(p->d2h);
   delete p;

@@ -32,10 +32,10 @@ ERRORS = {
 }
 
 EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_set_weight_decay", "lopt_step",
-            "lopt_step_host",
+            "lopt_step_host", "lopt_host_sync",
             "lopt_shard_sizes", "lopt_shard_begin", "lopt_shard_middle", "lopt_shard_end",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
-            "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_version")
+            "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_last_cuda_error", "lopt_version")
 
 
 class LoptTensor(ctypes.Structure):
@@ -80,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_step_host.restype = i32
     lib.lopt_step_host.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
                                    i64, ctypes.c_float, vp]
+    lib.lopt_host_sync.restype = i32
+    lib.lopt_host_sync.argtypes = [vp, vp]
     lib.lopt_step.restype = i32
     lib.lopt_shard_sizes.argtypes = [ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.lopt_shard_sizes.restype = i32
@@ -103,6 +105,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_destroy.argtypes = [vp]
     lib.lopt_destroy.restype = i32
     lib.lopt_strerror.argtypes = [i32]
+    lib.lopt_last_cuda_error.restype = ctypes.c_char_p
+    lib.lopt_last_cuda_error.argtypes = []
     lib.lopt_strerror.restype = ctypes.c_char_p
     lib.lopt_version.argtypes = []
     lib.lopt_version.restype = i32
@@ -112,7 +116,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def _check(fn: str, code: int) -> None:
     if code != LOPT_OK:
-        raise LoptError(fn, code, load_library().lopt_strerror(code).decode())
+        lib = load_library()
+        msg = lib.lopt_strerror(code).decode()
+        if code in (-4, -5):   # LOPT_E_CUDA, LOPT_E_OOM: name the CUDA error
+            msg += " [%s]" % lib.lopt_last_cuda_error().decode()
+        raise LoptError(fn, code, msg)
 
 
 def _ptr(t, n: int, what: str) -> int:
@@ -238,11 +246,13 @@ class LearnedOptimizer:
     def step_host(self, tensors, grad_host, param_host, t: int, lr: float = 1.0,
                   stream: Optional[object] = None) -> None:
         """One step with gradients coming from and parameters going to host
-        memory: grad_host[i] is copied into tensor i's device gradient before
-        its step and the new parameters into param_host[i] after it (CPU
+        memory: grad_host[i] is tensor i's gradient (its device ``grad`` is
+        not used) and the new parameters are copied into param_host[i] (CPU
         float32 buffers of rows * cols elements; pinned memory lets the
-        copies overlap the kernels).  Asynchronous on ``stream``; the host
-        buffers are complete once the stream has passed this call."""
+        copies overlap the kernels).  The kernels are asynchronous on
+        ``stream``; the parameter copies may still run after it: call
+        ``host_sync`` (or ``check``) before reading param_host or refilling
+        grad_host."""
         pl = tensors if isinstance(tensors, PreparedList) else self.prepare(tensors)
         if len(grad_host) != pl.n or len(param_host) != pl.n:
             raise ValueError("one host gradient and one host parameter buffer per tensor")
@@ -252,6 +262,11 @@ class LearnedOptimizer:
                                         for i, (x, ts) in enumerate(zip(param_host, pl.tensors))])
         _check("lopt_step_host", load_library().lopt_step_host(self._h, pl.array, pl.n, gp, pp, int(t), float(lr),
                                                                 self._stream(stream)))
+
+    def host_sync(self, stream: Optional[object] = None) -> None:
+        """Make ``stream`` wait for every parameter copy of the host-buffer
+        steps enqueued so far."""
+        _check("lopt_host_sync", load_library().lopt_host_sync(self._h, self._stream(stream)))
 
     # ---- row-sharded step --------------------------------------------------
     @staticmethod
