@@ -171,11 +171,11 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
  *
  * Per tensor the step is the same computation as lopt_step() (every
  * normalisation statistic belongs to one tensor), so results are
- * identical.  The list is cut into up to 8 groups of consecutive tensors of
- * about equal size (at least 4 Mi elements each), each stepped by its own
- * three launches on `stream`; the copies run on two streams of the handle,
- * so that gradient and parameter copies overlap the kernels of other
- * groups, also across consecutive calls.  Adjacent tensors whose buffers
+ * identical.  The list is cut into up to 2 groups (lopt_set_host_groups)
+ * of consecutive tensors of about equal size (at least 4 Mi elements
+ * each), each stepped by its own three launches on `stream`; the copies
+ * run on two streams of the handle, so that gradient and parameter copies
+ * overlap the kernels of other groups, also across consecutive calls.  Adjacent tensors whose buffers
  * follow each other on both sides move in one copy.
  *
  * Ordering.  The kernels are ordered with other work on `stream`.  The
@@ -210,6 +210,16 @@ int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors,
  * Errors: LOPT_E_ARG (NULL handle), LOPT_E_CUDA.
  */
 int lopt_host_sync(lopt_handle h, void* stream);
+
+/*
+ * Most groups of tensors a host-buffer step of this handle uses (1..16;
+ * default 2).  One group runs the copies and the kernels one after the
+ * other; with more, the copies of one group overlap the kernels of
+ * another, but each group adds three launches and their start and end.
+ * Takes effect on the next lopt_step_host() call.  Errors: LOPT_E_ARG (NULL handle or a
+ * value out of range).
+ */
+int lopt_set_host_groups(lopt_handle h, int max_groups);
 
 /*
  * ---- Row-sharded step (data parallel over ranks) --------------------------

@@ -84,6 +84,7 @@ struct lopt_ctx {
   // the parts share the parent's weights
   HostPipe* pipe = nullptr;
   bool shared_weights = false;
+  int host_groups = 2;           // most groups of a host-buffer step (lopt_set_host_groups)
   // optional per-kernel timing: 4 events per timed step
   bool timing = false;
   std::vector<cudaEvent_t> tev;
@@ -325,7 +326,7 @@ int leave_phase(lopt_ctx* h, cudaStream_t stream, cudaError_t e) {
 }  // namespace
 
 // ---- host-buffer steps ------------------------------------------------------
-constexpr int kHostGroups = 8;                 // most groups of tensors per step
+constexpr int kHostGroupsMax = 16;             // most groups of tensors per step
 constexpr int64_t kHostGroupElems = 1 << 22;   // fewest elements per group
 
 // Consecutive calls alternate between two device staging buffers for the
@@ -349,13 +350,13 @@ constexpr int kGroupEvents = 5;
 
 namespace {
 
-// Consecutive groups of about equal element counts: up to kHostGroups, at
+// Consecutive groups of about equal element counts: up to max_groups, at
 // least kHostGroupElems elements each (one group for a small list), at
 // least one tensor each.
-void split_groups(const lopt_tensor* ts, int n, std::vector<int>& split) {
+void split_groups(const lopt_tensor* ts, int n, int max_groups, std::vector<int>& split) {
   int64_t total = 0;
   for (int i = 0; i < n; ++i) total += ts[i].rows * ts[i].cols;
-  int G = (int)std::min<int64_t>(kHostGroups, std::max<int64_t>(1, total / kHostGroupElems));
+  int G = (int)std::min<int64_t>(max_groups, std::max<int64_t>(1, total / kHostGroupElems));
   G = std::min(G, n);
   split.assign(1, 0);
   int64_t acc = 0;
@@ -663,7 +664,7 @@ int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors, con
       for (int i = 0; i < n_tensors; ++i) p->staged[q][i].grad = p->stage[q] + off[i];
       if ((rc = validate(h, p->staged[q].data(), n_tensors)) != LOPT_OK) return rc;
     }
-    split_groups(tensors, n_tensors, p->split);
+    split_groups(tensors, n_tensors, h->host_groups, p->split);
     const int G = (int)p->split.size() - 1;
     for (int q = 0; q < 2; ++q) {
       while ((int)p->parts[q].size() < G) {
@@ -759,6 +760,15 @@ int lopt_step_host(lopt_handle h, const lopt_tensor* tensors, int n_tensors, con
     p->any = true;
   }
   return leave_phase(h, stream, e);
+}
+
+int lopt_set_host_groups(lopt_handle h, int max_groups) {
+  if (!h || max_groups < 1 || max_groups > kHostGroupsMax || h->shared_weights) return LOPT_E_ARG;
+  if (max_groups != h->host_groups) {
+    h->host_groups = max_groups;
+    if (h->pipe) h->pipe->list.clear();   // split again on the next call
+  }
+  return LOPT_OK;
 }
 
 int lopt_host_sync(lopt_handle h, void* stream_ptr) {

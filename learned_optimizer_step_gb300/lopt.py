@@ -32,7 +32,7 @@ ERRORS = {
 }
 
 EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_set_weight_decay", "lopt_step",
-            "lopt_step_host", "lopt_host_sync",
+            "lopt_step_host", "lopt_host_sync", "lopt_set_host_groups",
             "lopt_shard_sizes", "lopt_shard_begin", "lopt_shard_middle", "lopt_shard_end",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
             "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_last_cuda_error", "lopt_version")
@@ -82,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                    i64, ctypes.c_float, vp]
     lib.lopt_host_sync.restype = i32
     lib.lopt_host_sync.argtypes = [vp, vp]
+    lib.lopt_set_host_groups.restype = i32
+    lib.lopt_set_host_groups.argtypes = [vp, i32]
     lib.lopt_step.restype = i32
     lib.lopt_shard_sizes.argtypes = [ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     lib.lopt_shard_sizes.restype = i32
@@ -262,6 +264,10 @@ class LearnedOptimizer:
                                         for i, (x, ts) in enumerate(zip(param_host, pl.tensors))])
         _check("lopt_step_host", load_library().lopt_step_host(self._h, pl.array, pl.n, gp, pp, int(t), float(lr),
                                                                 self._stream(stream)))
+
+    def set_host_groups(self, max_groups: int) -> None:
+        """Most groups of tensors a host-buffer step uses (1..16; default 2)."""
+        _check("lopt_set_host_groups", load_library().lopt_set_host_groups(self._h, int(max_groups)))
 
     def host_sync(self, stream: Optional[object] = None) -> None:
         """Make ``stream`` wait for every parameter copy of the host-buffer

@@ -74,6 +74,7 @@ def test_validation_before_any_device_call(lib):
     assert lib.lopt_step(None, None, 0, 1, 1.0, None) == -1
     assert lib.lopt_step_host(None, None, 0, None, None, 1, 1.0, None) == -1
     assert lib.lopt_host_sync(None, None) == -1
+    assert lib.lopt_set_host_groups(None, 4) == -1
     assert isinstance(lib.lopt_last_cuda_error(), bytes)
     assert lib.lopt_check(None) == -1
     assert lib.lopt_destroy(None) == -1

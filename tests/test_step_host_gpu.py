@@ -16,8 +16,8 @@ from tests.gpu_helpers import TOL_FP32, TOL_TC, cpu, elem_tol, make_states, need
 
 pytestmark = pytest.mark.gpu
 
-# about 21 Mi elements: five groups of at least 4 Mi elements, with ragged
-# and small tensors between the large ones
+# about 21 Mi elements: up to five groups of at least 4 Mi elements, with
+# ragged and small tensors between the large ones
 BIG = [("w%d" % i, (1024, 2048)) for i in range(9)] + [("b", (2048,)), ("odd", (37, 1001)),
                                                       ("w9", (1536, 1366)), ("v", (7,))]
 SMALL = [("a", (96, 130)), ("b", (257,)), ("c", (40, 64)), ("d", (7, 5))]
@@ -70,16 +70,18 @@ def test_host_step_equals_device_step_bitwise(path):
             assert torch.equal(sa["rms"], sb["rms"])
 
 
-@pytest.mark.parametrize("path", ["fp32", "tc"])
-def test_back_to_back_host_steps_equal_device_steps(path):
+@pytest.mark.parametrize("path,groups", [("fp32", 2), ("tc", 2), ("tc", 1), ("tc", 16)])
+def test_back_to_back_host_steps_equal_device_steps(path, groups):
     """Four host steps enqueued without a sync in between (the copies of one
     call overlap the kernels of the next, the staging buffers alternate),
-    each with its own host buffers, against four lopt_step calls."""
+    each with its own host buffers, against four lopt_step calls; with one
+    group, the default, and more groups than the list allows."""
     torch = need_gpu()
     a = make_states(BIG, recipe="vit", seed=26)
     b = make_states(BIG, recipe="vit", seed=26)
     ea, _ = _engine(path)
     eb, _ = _engine(path)
+    eb.set_host_groups(groups)
     steps = []
     for t in (1, 2, 3, 4):
         gen = torch.Generator(device="cuda").manual_seed(200 + t)
@@ -152,6 +154,16 @@ def test_host_step_weight_decay_and_path_follow_the_handle():
     torch.cuda.synchronize()
     for sa, sb in zip(a2, b2):
         assert torch.equal(sa["param"], sb["param"])
+
+
+def test_host_groups_rejects_bad_values():
+    need_gpu()
+    from learned_optimizer_step_gb300 import LoptError
+    eng, _ = _engine("fp32")
+    for bad in (0, -1, 17):
+        with pytest.raises(LoptError):
+            eng.set_host_groups(bad)
+    eng.set_host_groups(16)
 
 
 def test_host_step_rejects_bad_buffers():
