@@ -23,9 +23,12 @@
 //                the b2 preset of its accumulator; then for each tile
 //                ReLU(h2), the two-unit output layer in FP32 on the CUDA
 //                cores, and the update of p in the stage.
-// A tile is 128 consecutive elements of one tensor (one per TMEM lane).  A
-// tile slot is a set of tensor-memory columns: the FP32 accumulator (NP
-// columns) and the FP16 A operand of the next MMA (16 columns); the A
+// A tile is 128 elements of one tensor (one per TMEM lane); four tiles
+// cover 512 consecutive elements, lane t of each holding one of elements
+// 4t..4t+3, so that a feature thread finds the row of four consecutive
+// elements once and loads them in pairs.  A tile slot is a set of
+// tensor-memory columns: the FP32 accumulator (NP columns) and the FP16 A
+// operand of the next MMA (16 columns); the A
 // operands never pass through shared memory.  Per-tensor data (scales,
 // 1/rho, row/column accumulator addresses) travel with each stage in a
 // small record, so the feature warps keep no per-tensor state.  Owning whole
@@ -108,6 +111,9 @@ struct StageRec {
   int32_t      C;
   uint32_t     bytes;        // bytes per array; 0: not staged (nothing to write back)
   float        invC;         // 1 / C
+  int32_t      quad;         // staged, C % 4 == 0 and the column accumulators 16-byte aligned:
+                             // the four elements of a lane share a row, c is read in pairs
+  int32_t      pad_[3];
 };
 static_assert(sizeof(StageRec) % 16 == 0, "stage records stay 16-byte aligned");
 
@@ -135,10 +141,22 @@ struct Geom {
   static_assert(Smem <= 232448, "shared memory of one CTA");
   // an epilogue group finishes layer 1 of all tiles of a stage before the
   // rest of any: the stage's last tile must not wait for a slot of its own
-  static_assert(S * SlotCols <= 512 && S >= kStageTiles && kDone >= kEpiGroups * kStageTiles + S,
+  // a feature thread holds back the announcement of one tile while it waits
+  // for the next tile's slot: that slot must not wait for the held tile's stage
+  static_assert(S * SlotCols <= 512 && S > kStageTiles && kDone >= kEpiGroups * kStageTiles + S,
                 "tensor memory columns / pipeline depth");
   static_assert(oRec % 16 == 0 && sizeof(StageRec) % 16 == 0, "16-byte aligned stage records");
 };
+
+// Element layout of a stage: its tiles go in groups of four (a quad, 512
+// consecutive elements); lane t of tile 4q + e holds element 512q + 4t + e,
+// so that one thread builds the features of four consecutive elements from
+// 64-bit loads and shares their row terms.  A stage of n elements has
+// 4 * ceil(n / 512) tiles.
+constexpr int kQuadElems = 4 * kTile;
+static_assert(kStageElems % kQuadElems == 0 && kApplyChunk % kStageElems == 0,
+              "units are whole stages but the last, stages whole quads but the last");
+__device__ __forceinline__ int32_t stage_tiles(int32_t n) { return ((n + kQuadElems - 1) / kQuadElems) * 4; }
 
 // Walks the stages of a session in order.  A stage holds up to kStageTiles
 // consecutive tiles of one work unit; stage n of a session lives in ring
@@ -167,7 +185,7 @@ struct StageIter {
   }
   __device__ bool valid() const { return u < u1; }
   __device__ void next() {
-    k0 += (n + kTile - 1) / kTile;
+    k0 += stage_tiles(n);
     soff += kStageElems;
     if (soff >= ulen) {
       ++u;
@@ -182,8 +200,8 @@ struct StageIter {
 __device__ __forceinline__ int32_t unit_tiles(const StepArgs& a, int32_t u) {
   const Unit x = a.units[u];
   const int64_t st = (int64_t)x.local * kApplyChunk;
-  const int64_t en = min(a.desc[x.tensor].N, st + (int64_t)kApplyChunk);
-  return (int32_t)((en - st + kTile - 1) / kTile);
+  const int32_t len = (int32_t)min(a.desc[x.tensor].N - st, (int64_t)kApplyChunk);
+  return (len / kStageElems) * stage_tiles(kStageElems) + stage_tiles(len % kStageElems);
 }
 
 // Bounded wait that ignores the abort flag (used to drain in-flight work).
@@ -205,24 +223,59 @@ __device__ __forceinline__ void pack_relu_row(const uint32_t (&h)[NP], uint32_t 
     av[q] = 2 * q < NP ? relu_f16x2(__uint_as_float(h[2 * q]), __uint_as_float(h[2 * q + 1])) : 0u;
 }
 
+// Row and column of the element at offset xi of a stage: j0 + xi < C +
+// kStageElems, so a float quotient is exact to within one.
+__device__ __forceinline__ void stage_row_col(const StageRec& rc, int xi, int64_t& i, uint32_t& jc) {
+  const uint32_t C = (uint32_t)rc.C;
+  i = rc.i0;
+  jc = (uint32_t)rc.j0 + (uint32_t)xi;
+  if (jc >= C) {
+    uint32_t q = (uint32_t)((float)jc * rc.invC);
+    int32_t rem = (int32_t)(jc - q * C);
+    if (rem < 0) { --q; rem += (int32_t)C; }
+    else if (rem >= (int32_t)C) { ++q; rem -= (int32_t)C; }
+    i += q;
+    jc = (uint32_t)rem;
+  }
+}
+
+__device__ __forceinline__ float2 ld_f2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ void st_f2(float* p, const float2& v) { *reinterpret_cast<float2*>(p) = v; }
+// Component e of a float2 (e a constant after unrolling).
+__device__ __forceinline__ float f2get(const float2& v, int e) { return e == 0 ? v.x : v.y; }
+__device__ __forceinline__ void f2set(float2& v, int e, float x) {
+  if (e == 0) v.x = x;
+  else v.y = x;
+}
+
+// Per-row terms of one element's features: rr = r / rho and sr = sqrt(r)
+// (as r * rsqrt(r + eps)), shared by every element of a row.
+__device__ __forceinline__ void row_terms_f16(const float (&r)[3], const float (&inv_rho)[3], float (&rr)[3],
+                                              float (&sr)[3]) {
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    rr[k] = fmul(r[k], inv_rho[k]);
+    sr[k] = fmul(r[k], frsqrt(fadd(r[k], kEps)));
+  }
+}
+
 // The accumulator update and the 28 features of one element, normalised by
 // the scales sc and packed as FP16 pairs (feature order as in lopt_features).
 // m and v get exactly lopt_features' arithmetic (they are stored); the
 // features themselves, which go to FP16, use paired FP32 multiplies where two
 // neighbouring features share the operation, and a fused multiply-add
-// inside rsqrt(r c / rho + eps).
-__device__ __forceinline__ void features_f16(float p, float g, float (&m)[3], float& v, const float (&r)[3],
-                                             const float (&c)[3], const float (&inv_rho)[3], const float* sc,
+// inside rsqrt(r c / rho + eps).  rr, sr: the element's row terms.
+__device__ __forceinline__ void features_f16(float p, float g, float (&m)[3], float& v, const float (&rr)[3],
+                                             const float (&sr)[3], const float (&c)[3], const float* sc,
                                              uint32_t (&av)[16]) {
 #pragma unroll
   for (int k = 0; k < 3; ++k) m[k] = ffma(beta(k), m[k], fmul(one_minus_beta(k), g));
   v = ffma(kBeta2, v, fmul(kOneMinusBeta2, fmul(g, g)));
   const float rsv = frsqrt(fadd(v, kEps));
-  float rvh[3], sr[3], sq[3];
+  float rvh[3], sq[3];
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
-    rvh[k] = frsqrt(fmaf(fmul(r[k], inv_rho[k]), c[k], kEps));
-    sr[k] = fmul(r[k], frsqrt(fadd(r[k], kEps)));
+    rvh[k] = frsqrt(fmaf(rr[k], c[k], kEps));
     sq[k] = fmul(c[k], frsqrt(fadd(c[k], kEps)));
   }
   float2 q[14];
@@ -249,6 +302,8 @@ __device__ __forceinline__ void features_f16(float p, float g, float (&m)[3], fl
     av[2 * k] = f16x2(lo.x, lo.y);
     av[2 * k + 1] = f16x2(hi.x, hi.y);
   }
+  av[14] = 0x00003C00u;   // 1.0h (against b1 in the B operand), 0
+  av[15] = 0u;
 }
 
 template <int NP>
@@ -392,6 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
                 rc.C = (int32_t)d.C;
                 rc.invC = 1.0f / (float)d.C;
                 rc.bytes = stg ? bytes : 0u;
+                rc.quad = stg && (d.C & 3) == 0 &&
+                          (((uintptr_t)d.c[0] | (uintptr_t)d.c[1] | (uintptr_t)d.c[2]) & 15) == 0;
               }
               if (lane < 3) rc.c[lane] = d.c[lane];
               else if (lane < 6) rc.r[lane - 3] = d.r[lane - 3];
@@ -469,71 +526,121 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           const StageRec& rc = rec[si.st];
           const bool stg = rc.bytes != 0;
           float* const sbase = ring + si.st * (kArrays * kStageElems);
-          const int ntl = (si.n + kTile - 1) / kTile;
+          const int nq = stage_tiles(si.n) / 4;
           int s = si.k0 % S;                          // slot of the stage's first tile
           uint32_t sph = (uint32_t)((si.k0 / S) & 1);  // its round parity
-          for (int j = 0; j < ntl; ++j) {
-            const int x = j * kTile + t;                 // element offset in the stage
-            const int xi = min(x, si.n - 1);             // past the end: index math of the last element
-            float p, g, m[3], v;
-            if (stg) {   // elements past the end read and write unused stage words
-              p = sbase[x]; g = sbase[kStageElems + x]; m[0] = sbase[2 * kStageElems + x];
-              m[1] = sbase[3 * kStageElems + x]; m[2] = sbase[4 * kStageElems + x]; v = sbase[5 * kStageElems + x];
-            } else {
-              const TensorDesc& d = a.desc[rc.tensor];
-              const int64_t e = rc.e0 + xi;
-              p = d.p[e]; g = __ldg(d.g + e); v = d.v[e];
-#pragma unroll
-              for (int q = 0; q < 3; ++q) m[q] = d.m[q][e];
+          int held = -1;                              // slot whose A operand store is not yet announced
+          // Hands a tile's A operand to its slot.  The slot is waited for only
+          // now, so that loads and arithmetic overlap the wait; the store is
+          // waited for (and the layer-1 MMA thread told) at the next tile,
+          // after that tile's arithmetic.  Holding back one announcement
+          // cannot block a slot wait: the slot of tile k + 1 waits for tile
+          // k + 1 - S, whose stage ends before tile k (S > kStageTiles).
+          auto emit = [&](const uint32_t (&av)[16]) -> bool {
+            if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) return false;
+            if (held >= 0) {
+              tmem_wait_st();
+              tc_fence_before();
+              mbar_arrive(a1_full + held);
             }
-            // row and column of the element: j0 + xi < C + kStageElems, so a
-            // float quotient is exact to within one
-            const uint32_t C = (uint32_t)rc.C;
-            int64_t i = rc.i0;
-            uint32_t jc = (uint32_t)rc.j0 + (uint32_t)xi;
-            if (jc >= C) {
-              uint32_t q = (uint32_t)((float)jc * rc.invC);
-              int32_t rem = (int32_t)(jc - q * C);
-              if (rem < 0) { --q; rem += (int32_t)C; }
-              else if (rem >= (int32_t)C) { ++q; rem -= (int32_t)C; }
-              i += q;
-              jc = (uint32_t)rem;
-            }
-            float c[3], r[3];
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-              c[q] = __ldg(rc.c[q] + jc);
-              r[q] = __ldg(rc.r[q] + i);
-            }
-            float inv_rho[3];
-#pragma unroll
-            for (int q = 0; q < 3; ++q) inv_rho[q] = rc.inv_rho[q];
-            // normalised features, FP16, for this lane's row of the slot's A
-            // operand in tensor memory (K = 32: 28 features, 1 for the bias, 0s)
-            uint32_t av[16];
-            features_f16(p, g, m, v, r, c, inv_rho, rc.sc, av);
-            if (stg) {
-              sbase[2 * kStageElems + x] = m[0]; sbase[3 * kStageElems + x] = m[1];
-              sbase[4 * kStageElems + x] = m[2]; sbase[5 * kStageElems + x] = v;
-            } else if (x < si.n) {
-              const TensorDesc& d = a.desc[rc.tensor];
-              const int64_t e = rc.e0 + x;
-#pragma unroll
-              for (int q = 0; q < 3; ++q) d.m[q][e] = m[q];
-              d.v[e] = v;
-            }
-            av[14] = 0x00003C00u;   // 1.0h, 0
-            av[15] = 0u;
-            // the tile's slot is needed only now: loads and arithmetic above
-            // overlap the wait for it
-            if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) { ok = false; break; }
             tmem_st16(t_lane + s * G::SlotCols + NP, av);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(a1_full + s);
+            held = s;
             if (++s == S) { s = 0; sph ^= 1u; }
+            return true;
+          };
+          for (int qd = 0; ok && qd < nq; ++qd) {
+            const int x0 = qd * kQuadElems + 4 * t;   // this lane's first element in the stage
+            if (rc.quad) {
+              // four consecutive elements of one row (C % 4 == 0 and x0 % 4 ==
+              // 0); past the end: unused stage words, and the row and columns
+              // of the stage's last four elements
+              int64_t i;
+              uint32_t jc;
+              stage_row_col(rc, min(x0, si.n - 4), i, jc);
+              float r[3], inv_rho[3], rr[3], sr[3];
+#pragma unroll
+              for (int q = 0; q < 3; ++q) {
+                r[q] = __ldg(rc.r[q] + i);
+                inv_rho[q] = rc.inv_rho[q];
+              }
+              row_terms_f16(r, inv_rho, rr, sr);
+              // two pairs of elements, 64-bit loads and stores
+#pragma unroll
+              for (int h = 0; h < 4; h += 2) {
+                const int xh = x0 + h;
+                const float2 P = ld_f2(sbase + xh), Gr = ld_f2(sbase + kStageElems + xh);
+                float2 M0 = ld_f2(sbase + 2 * kStageElems + xh), M1 = ld_f2(sbase + 3 * kStageElems + xh);
+                float2 M2 = ld_f2(sbase + 4 * kStageElems + xh), V = ld_f2(sbase + 5 * kStageElems + xh);
+                float2 c2[3];
+#pragma unroll
+                for (int q = 0; q < 3; ++q) c2[q] = __ldg(reinterpret_cast<const float2*>(rc.c[q] + jc + h));
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  float m[3] = {f2get(M0, e), f2get(M1, e), f2get(M2, e)};
+                  float v = f2get(V, e);
+                  const float c[3] = {f2get(c2[0], e), f2get(c2[1], e), f2get(c2[2], e)};
+                  // normalised features, FP16, for this lane's row of the A
+                  // operand of tile 4 qd + h + e (K = 32: 28 features, 1, 0s)
+                  uint32_t av[16];
+                  features_f16(f2get(P, e), f2get(Gr, e), m, v, rr, sr, c, rc.sc, av);
+                  f2set(M0, e, m[0]); f2set(M1, e, m[1]); f2set(M2, e, m[2]); f2set(V, e, v);
+                  if (!emit(av)) { ok = false; break; }
+                }
+                if (!ok) break;
+                st_f2(sbase + 2 * kStageElems + xh, M0); st_f2(sbase + 3 * kStageElems + xh, M1);
+                st_f2(sbase + 4 * kStageElems + xh, M2); st_f2(sbase + 5 * kStageElems + xh, V);
+              }
+              if (!ok) break;
+            } else {
+#pragma unroll 1
+              for (int e = 0; e < 4; ++e) {
+                const int x = x0 + e;                // element offset in the stage
+                const int xi = min(x, si.n - 1);     // past the end: index math of the last element
+                float p, g, m[3], v;
+                if (stg) {   // elements past the end read and write unused stage words
+                  p = sbase[x]; g = sbase[kStageElems + x]; m[0] = sbase[2 * kStageElems + x];
+                  m[1] = sbase[3 * kStageElems + x]; m[2] = sbase[4 * kStageElems + x];
+                  v = sbase[5 * kStageElems + x];
+                } else {
+                  const TensorDesc& d = a.desc[rc.tensor];
+                  const int64_t el = rc.e0 + xi;
+                  p = d.p[el]; g = __ldg(d.g + el); v = d.v[el];
+#pragma unroll
+                  for (int q = 0; q < 3; ++q) m[q] = d.m[q][el];
+                }
+                int64_t i;
+                uint32_t jc;
+                stage_row_col(rc, xi, i, jc);
+                float c[3], r[3], inv_rho[3], rr[3], sr[3];
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                  c[q] = __ldg(rc.c[q] + jc);
+                  r[q] = __ldg(rc.r[q] + i);
+                  inv_rho[q] = rc.inv_rho[q];
+                }
+                row_terms_f16(r, inv_rho, rr, sr);
+                uint32_t av[16];
+                features_f16(p, g, m, v, rr, sr, c, rc.sc, av);
+                if (stg) {
+                  sbase[2 * kStageElems + x] = m[0]; sbase[3 * kStageElems + x] = m[1];
+                  sbase[4 * kStageElems + x] = m[2]; sbase[5 * kStageElems + x] = v;
+                } else if (x < si.n) {
+                  const TensorDesc& d = a.desc[rc.tensor];
+                  const int64_t el = rc.e0 + x;
+#pragma unroll
+                  for (int q = 0; q < 3; ++q) d.m[q][el] = m[q];
+                  d.v[el] = v;
+                }
+                if (!emit(av)) { ok = false; break; }
+              }
+            }
           }
           if (!ok) break;
+          if (held >= 0) {
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(a1_full + held);
+          }
           fence_proxy_async();   // m, v in the stage, before its write-back
           mbar_arrive(stage_done + si.st);
         }
@@ -560,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           if (ns % kEpiGroups != h) continue;
           // the stage's record (written by the producer before it was loaded)
           if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
-          const int ntl = (si.n + kTile - 1) / kTile;
+          const int ntl = stage_tiles(si.n);
           const int s0 = si.k0 % S;
           // ---- layer 1 of every tile
           int s = s0;
@@ -647,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             float ex;
             asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
             const float upd = o0 * ex * kOutScale;
-            const int x = j * kTile + t;
+            const int x = (j >> 2) * kQuadElems + 4 * t + (j & 3);   // this lane's element of tile j
             if (stg) {   // past the end: an unused stage word
               pst[x] = pst[x] - lr * (upd + wd * pst[x]);
             } else if (x < si.n) {
