@@ -701,65 +701,76 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             if (++s == S) s = 0;
           }
           if (!ok) break;
-          // ---- the rest of every tile; a slot is freed as soon as h2 is read
+          // ---- the rest of every tile, two tiles at a time (a stage has a
+          // multiple of four), so that every output-layer weight read from
+          // shared memory serves two elements; a slot is freed as soon as its
+          // h2 is read
           const StageRec& rc = rec[si.st];
           const bool stg = rc.bytes != 0;
           float* const pst = ring + si.st * (kArrays * kStageElems);
           s = s0;
-          for (int j = 0; j < ntl; ++j) {
+          for (int j = 0; j < ntl; j += 2) {
             const int32_t k = si.k0 + j;
-            if (!mbar_wait_or_abort(done2 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
+            if (!mbar_wait_or_abort(done2 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag) ||
+                !mbar_wait_or_abort(done2 + ((k + 1) & (kDone - 1)), (uint32_t)(((k + 1) / kDone) & 1), kWaitNs,
+                                    abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            uint32_t h2[NP];
-            tmem_ld_row<NP>(t_lane + s * G::SlotCols, h2);
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(slot_empty + s);
-            if (++s == S) s = 0;
-            // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3, in
-            // chunks of 8 hidden units whose weights are loaded one chunk
-            // ahead (shared-memory latency off the FMA chains)
-            constexpr int kCh = NP / 8;
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                             make_float2(0.f, 0.f)};   // (o0, o1) x 2 chains
-            float4 wcur[4], wnext[4];
+            const int s1 = s + 1 == S ? 0 : s + 1;
+            // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3 for
+            // both tiles, over 16 hidden units at a time, two FMA chains each
+            float2 acc[2][4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) wcur[q] = w3[q];
+            for (int q = 0; q < 4; ++q) acc[0][q] = acc[1][q] = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int ch = 0; ch < kCh; ++ch) {
-              if (ch + 1 < kCh) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) wnext[q] = w3[4 * (ch + 1) + q];
+            for (int hf = 0; hf < NP / 16; ++hf) {
+              uint32_t ha[16], hb[16];
+              tmem_ld16(t_lane + s * G::SlotCols + 16 * hf, ha);
+              tmem_ld16(t_lane + s1 * G::SlotCols + 16 * hf, hb);
+              tmem_wait_ld();
+              if (hf == NP / 16 - 1) {
+                tc_fence_before();
+                mbar_arrive(slot_empty + s);
+                mbar_arrive(slot_empty + s1);
               }
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int u = 8 * ch + 2 * q;
-                const float2 hr = make_float2(fmaxf(__uint_as_float(h2[u]), 0.f),
-                                              fmaxf(__uint_as_float(h2[u + 1]), 0.f));
-                acc[(q & 1) * 2] = __ffma2_rn(hr, make_float2(wcur[q].x, wcur[q].y), acc[(q & 1) * 2]);
-                acc[(q & 1) * 2 + 1] = __ffma2_rn(hr, make_float2(wcur[q].z, wcur[q].w), acc[(q & 1) * 2 + 1]);
-              }
-              if (ch + 1 < kCh) {
+              for (int ch = 0; ch < 2; ++ch) {   // 8 hidden units
+                float4 w[4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) wcur[q] = wnext[q];
+                for (int q = 0; q < 4; ++q) w[q] = w3[4 * (2 * hf + ch) + q];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  const int u = 8 * ch + 2 * q;
+                  const float2 w0 = make_float2(w[q].x, w[q].y), w1 = make_float2(w[q].z, w[q].w);
+                  const float2 ra = make_float2(fmaxf(__uint_as_float(ha[u]), 0.f), fmaxf(__uint_as_float(ha[u + 1]), 0.f));
+                  const float2 rb = make_float2(fmaxf(__uint_as_float(hb[u]), 0.f), fmaxf(__uint_as_float(hb[u + 1]), 0.f));
+                  acc[0][(q & 1) * 2] = __ffma2_rn(ra, w0, acc[0][(q & 1) * 2]);
+                  acc[0][(q & 1) * 2 + 1] = __ffma2_rn(ra, w1, acc[0][(q & 1) * 2 + 1]);
+                  acc[1][(q & 1) * 2] = __ffma2_rn(rb, w0, acc[1][(q & 1) * 2]);
+                  acc[1][(q & 1) * 2 + 1] = __ffma2_rn(rb, w1, acc[1][(q & 1) * 2 + 1]);
+                }
               }
             }
-            const float o0 = (acc[0].x + acc[0].y) + (acc[2].x + acc[2].y) + b30;
-            const float o1 = (acc[1].x + acc[1].y) + (acc[3].x + acc[3].y) + b31;
-            // exp(x) = 2^(x log2 e) with the PTX ex2.approx instruction
-            // (relative error below 2^-22); here |x| = |o1| * 1e-3 is small
-            float ex;
-            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
-            const float upd = o0 * ex * kOutScale;
-            const int x = (j >> 2) * kQuadElems + 4 * t + (j & 3);   // this lane's element of tile j
-            if (stg) {   // past the end: an unused stage word
-              pst[x] = pst[x] - lr * (upd + wd * pst[x]);
-            } else if (x < si.n) {
-              float* pp = a.desc[rc.tensor].p + (rc.e0 + x);
-              *pp = *pp - lr * (upd + wd * *pp);
+            s = s1 + 1 == S ? 0 : s1 + 1;
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+              const float o0 = (acc[tt][0].x + acc[tt][0].y) + (acc[tt][2].x + acc[tt][2].y) + b30;
+              const float o1 = (acc[tt][1].x + acc[tt][1].y) + (acc[tt][3].x + acc[tt][3].y) + b31;
+              // exp(x) = 2^(x log2 e) with the PTX ex2.approx instruction
+              // (relative error below 2^-22); here |x| = |o1| * 1e-3 is small
+              float ex;
+              asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ex) : "f"(o1 * (kOutScale * 1.44269504088896341f)));
+              const float upd = o0 * ex * kOutScale;
+              const int jt = j + tt;
+              const int x = (jt >> 2) * kQuadElems + 4 * t + (jt & 3);   // this lane's element of tile jt
+              if (stg) {   // past the end: an unused stage word
+                pst[x] = pst[x] - lr * (upd + wd * pst[x]);
+              } else if (x < si.n) {
+                float* pp = a.desc[rc.tensor].p + (rc.e0 + x);
+                *pp = *pp - lr * (upd + wd * *pp);
+              }
             }
           }
           if (!ok) break;

@@ -312,3 +312,25 @@ def test_weight_decay_rejects_bad_values():
     for bad in (-0.1, float("nan"), float("inf")):
         with pytest.raises(LoptError):
             eng.set_weight_decay(bad)
+
+
+@pytest.mark.parametrize("path,tol", PATHS)
+def test_misaligned_column_accumulators(path, tol):
+    """Column accumulators 4 bytes off a 16-byte boundary: the kernels take
+    their scalar routes for these tensors (the tensor-core apply kernel its
+    per-element one instead of four elements per lane); parity with the
+    oracle as for aligned buffers."""
+    torch = need_gpu()
+    eng, w = engine(path=path)
+    states = make_states([("w", (64, 96)), ("b", (1000,)), ("h", (5, 1000))], recipe="vit", seed=12)
+    for st in states:
+        cols = []
+        for c in st["col"]:
+            buf = torch.zeros(c.numel() + 1, device=c.device, dtype=c.dtype)
+            view = buf[1:]
+            view.copy_(c)
+            cols.append(view)
+        st["col"] = cols
+    assert all(c.data_ptr() % 16 == 4 for st in states for c in st["col"])
+    for t in (1, 2):
+        compare_step(eng, states, w, 32, t, 1.0, tol)
