@@ -669,24 +669,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
           const int ntl = stage_tiles(si.n);
           const int s0 = si.k0 % S;
-          // ---- layer 1 of every tile
+          // ---- layer 1 of every tile, two tiles at a time: the b2 preset is
+          // read from shared memory once for both
           int s = s0;
-          for (int j = 0; j < ntl; ++j) {
-            const int32_t k = si.k0 + j;
-            if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
-              ok = false;
-              break;
+          for (int j = 0; j < ntl; j += 2) {
+            const int s1 = s + 1 == S ? 0 : s + 1;
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+              const int32_t k = si.k0 + j + tt;
+              if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t col = t_lane + (tt ? s1 : s) * G::SlotCols;
+              uint32_t av[16];
+              {
+                uint32_t h1[NP];
+                tmem_ld_row<NP>(col, h1);
+                tmem_wait_ld();
+                pack_relu_row<NP>(h1, av);
+              }
+              tmem_st16(col + NP, av);
             }
-            tc_fence_after();
-            const uint32_t col = t_lane + s * G::SlotCols;
-            uint32_t av[16];
-            {
-              uint32_t h1[NP];
-              tmem_ld_row<NP>(col, h1);
-              tmem_wait_ld();
-              pack_relu_row<NP>(h1, av);
-            }
-            tmem_st16(col + NP, av);
+            if (!ok) break;
             uint32_t b2[NP];
 #pragma unroll
             for (int q = 0; q < NP; q += 4) {
@@ -694,11 +700,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
               b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
               b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
             }
-            tmem_st_row<NP>(col, b2);
+            tmem_st_row<NP>(t_lane + s * G::SlotCols, b2);
+            tmem_st_row<NP>(t_lane + s1 * G::SlotCols, b2);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(a2_full + s);
-            if (++s == S) s = 0;
+            mbar_arrive(a2_full + s1);
+            s = s1 + 1 == S ? 0 : s1 + 1;
           }
           if (!ok) break;
           // ---- the rest of every tile, two tiles at a time (a stage has a
