@@ -413,7 +413,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (value / world / PAGE_VIT_PARAMS_PER_S) if args.workload == "vit_b16" else None,
-        "dtype": "tf32/f16 mma, f32 accumulate" if path == "tc" else "f32",
+        "dtype": "f32 state, f16 mma operands, f32 accumulate" if path == "tc" else "f32",
         "data": "synthetic",
         "config": {"workload": "%s (%d fp32 tensors, %d params per GPU)" % (args.workload, len(states), numel),
                    "mlp": "39->%d->%d->2, %s path" % (wl.hidden, wl.hidden, path),
