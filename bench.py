@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -233,12 +234,21 @@ def flat_states(wl, device, seed=0):
     return states, flat, n
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank space, so that a change of
+    comments alone keeps a traffic record valid."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha(path: str) -> str:
-    """Hash of a kernel's source and the headers it includes."""
+    """Hash of the code (comments left out) of a kernel's source and the
+    headers it includes."""
     h = hashlib.sha256()
     for name in (path, "lopt_internal.cuh", "tc_layout.cuh"):
-        with open(os.path.join(ROOT, "learned_optimizer_step_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "learned_optimizer_step_gb300", "csrc", name), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

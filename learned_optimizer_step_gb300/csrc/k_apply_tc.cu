@@ -3,8 +3,8 @@
 // Same computation as the FP32 apply kernel ("PyLO: Towards Accessible
 // Learned Optimizers in PyTorch", section "融合カーネル戦略", kernel 2:
 // features recomputed in registers, normalised, MLP, update written back),
-// but the three MLP layers run as batched GEMMs on the 5th-generation tensor
-// cores: the page's design evaluates the MLP on CUDA cores with __ldg
+// but the two hidden layers run as batched GEMMs on the 5th-generation
+// tensor cores: the page's design evaluates the MLP on CUDA cores with __ldg
 // weights, which on GB300 is ALU-bound (about 4.7 kFLOP per element against
 // 44 bytes of traffic).
 //
@@ -18,9 +18,9 @@
 //                into the tile slot's tensor memory; the updated m and v go
 //                back into the stage;
 //   warps 17-18  MMA issuers, one thread each: layer 1 and layer 2;
-//   warps 0-7    two epilogue warpgroups, owning alternate stages: for each
-//                tile ReLU + FP16 A operand of layer 2 (in tensor memory) and
-//                the b2 preset of its accumulator; then for each tile
+//   warps 0-7    two epilogue warpgroups, owning alternate stages, two
+//                tiles at a time: ReLU + FP16 A operand of layer 2 (in
+//                tensor memory) and the b2 preset of its accumulator; then
 //                ReLU(h2), the two-unit output layer in FP32 on the CUDA
 //                cores, and the update of p in the stage.
 // A tile is 128 elements of one tensor (one per TMEM lane); four tiles
@@ -28,8 +28,8 @@
 // 4t..4t+3, so that a feature thread finds the row of four consecutive
 // elements once and loads them in pairs.  A tile slot is a set of
 // tensor-memory columns: the FP32 accumulator (NP columns) and the FP16 A
-// operand of the next MMA (16 columns); the A
-// operands never pass through shared memory.  Per-tensor data (scales,
+// operand of the next MMA (16 columns); the A operands never pass through
+// shared memory.  Per-tensor data (scales,
 // 1/rho, row/column accumulator addresses) travel with each stage in a
 // small record, so the feature warps keep no per-tensor state.  Owning whole
 // stages keeps the per-tile control flow of the warps small.
@@ -42,7 +42,12 @@
 // MMA round trips: the output layer (two units) runs on the CUDA cores.  The
 // two layers are issued by two threads in different warps, so that issuing
 // (a few dozen instructions per tile) is spread over two schedulers.  At
-// most S tiles are in flight (10 slots at NP = 32).
+// most S tiles are in flight (10 slots at NP = 32), and a tile keeps its
+// slot from its features to the read of its layer-2 result, so S tiles per
+// slot lifetime bound the throughput.  Most of that lifetime is the wait
+// for an epilogue group; hence the epilogue's two tiles at a time (shared
+// reads of b2 and W3), and hence no third MMA for the output layer: its
+// round trip lengthens the lifetime more than it shortens the epilogue.
 //
 // The tiles of a CTA are processed in sessions: maximal runs of tiles whose
 // tensors share one MLP weight set.  Between sessions the pipeline drains,
