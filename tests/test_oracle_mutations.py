@@ -1,5 +1,6 @@
-"""Plants plausible mistakes in the CPU oracle and checks that a pin catches
-each one.  Every mutation is applied by monkeypatching the oracle module for
+"""Plants plausible mistakes in the CPU oracle (constants, decays, indices,
+feature order, the MLP's biases, transposes and ReLUs, the update and the
+weight decay) and checks that a pin catches each one.  Every mutation is applied by monkeypatching the oracle module for
 the duration of one test; nothing here touches a GPU."""
 
 import numpy as np
@@ -103,7 +104,61 @@ def _sqrt_v_dropped(F):
     return F
 
 
+def _swap_features(a, b):
+    def f(F):
+        F = F.copy()
+        F[:, [a, b]] = F[:, [b, a]]
+        return F
+    return f
+
+
+def _row_col_blocks_swapped(F):
+    F = F.copy()
+    F[:, 13:16], F[:, 16:19] = F[:, 16:19].copy(), F[:, 13:16].copy()
+    return F
+
+
+def _vhat_without_rho(r, c, rho, i, j):
+    return r[i] * c[j]
+
+
+def _v_of_abs_g(g, mom, rms):
+    new_mom = [b * mom[k] + (1.0 - b) * g for k, b in enumerate(L.MOMENTUM_DECAYS)]
+    return new_mom, L.RMS_DECAY * rms + (1.0 - L.RMS_DECAY) * np.abs(g)
+
+
+def _momentum_weights_swapped(g, mom, rms):
+    new_mom = [(1.0 - b) * mom[k] + b * g for k, b in enumerate(L.MOMENTUM_DECAYS)]
+    return new_mom, L.RMS_DECAY * rms + (1.0 - L.RMS_DECAY) * g * g
+
+
+def _mlp_variant(drop_b1=False, drop_b2=False, drop_b3=False, w2_t=False, outputs_swapped=False):
+    def mlp(X, w):
+        h1 = np.maximum(X @ w.W1 + (0.0 if drop_b1 else w.b1), 0.0)
+        h2 = np.maximum(h1 @ (w.W2.T if w2_t else w.W2) + (0.0 if drop_b2 else w.b2), 0.0)
+        W3, b3 = (w.W3[:, ::-1], w.b3[::-1]) if outputs_swapped else (w.W3, w.b3)
+        return h2 @ W3 + (0.0 if drop_b3 else b3)
+    return mlp
+
+
 MUTATIONS = {
+    "epsilon 1e-8": ("EPS", 1e-8),
+    "time scales reversed": ("TIME_SCALES", tuple(reversed(L.TIME_SCALES))),
+    "v an EMA of |g|": ("accumulator_update", _v_of_abs_g),
+    "momentum weights beta and 1 - beta swapped": ("accumulator_update", _momentum_weights_swapped),
+    "vhat without 1 / rho": ("factored_vhat", _vhat_without_rho),
+    "sqrt(r) and sqrt(c) blocks swapped": ("features", _features_with(_row_col_blocks_swapped)),
+    "features p and g swapped": ("features", _features_with(_swap_features(0, 1))),
+    "features m_0 and m_2 swapped": ("features", _features_with(_swap_features(2, 4))),
+    "features m_0 rsqrt(v) and g rsqrt(vhat_0) swapped": ("features", _features_with(_swap_features(6, 10))),
+    "features g rsqrt(v) and g rsqrt(vhat_0) swapped": ("features", _features_with(_swap_features(9, 10))),
+    "features sqrt(r_0) and sqrt(r_2) swapped": ("features", _features_with(_swap_features(13, 15))),
+    "b1 dropped": ("mlp", _mlp_variant(drop_b1=True)),
+    "b2 dropped": ("mlp", _mlp_variant(drop_b2=True)),
+    "b3 dropped": ("mlp", _mlp_variant(drop_b3=True)),
+    "W2 read transposed": ("mlp", _mlp_variant(w2_t=True)),
+    "direction and magnitude swapped": ("mlp", _mlp_variant(outputs_swapped=True)),
+    "output scale 1e-2": ("OUTPUT_SCALE", 1e-2),
     "momentum decays reversed": ("MOMENTUM_DECAYS", (0.9, 0.5, 0.1)),
     "rms decay 0.99": ("RMS_DECAY", 0.99),
     "factored decays reversed": ("FACTORED_DECAYS", (0.9, 0.5, 0.1)),
