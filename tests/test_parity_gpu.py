@@ -334,3 +334,35 @@ def test_misaligned_column_accumulators(path, tol):
     assert all(c.data_ptr() % 16 == 4 for st in states for c in st["col"])
     for t in (1, 2):
         compare_step(eng, states, w, 32, t, 1.0, tol)
+
+
+def _with_biases(w, hidden, seed, scale=0.3):
+    """The weight sets w with seeded non-zero biases b1, b2, b3 (the sets
+    the other tests use have zero biases)."""
+    w = w.copy()
+    rng = np.random.default_rng(seed)
+    b1 = 39 * hidden
+    b2 = b1 + hidden + hidden * hidden
+    b3 = b2 + hidden + 2 * hidden
+    for s in range(w.shape[0]):
+        w[s, b1:b1 + hidden] = rng.normal(0.0, scale, hidden)
+        w[s, b2:b2 + hidden] = rng.normal(0.0, scale, hidden)
+        w[s, b3:b3 + 2] = rng.normal(0.0, scale, 2)
+    return w
+
+
+@pytest.mark.parametrize("path,tol", PATHS)
+@pytest.mark.parametrize("hidden", [4, 32])
+def test_nonzero_biases(hidden, path, tol):
+    """Every bias of the MLP non-zero: b1 (the tensor-core path takes it
+    through a constant column of layer 1's A operand), b2 and b3."""
+    need_gpu()
+    from learned_optimizer_step_gb300 import LearnedOptimizer
+    w = _with_biases(synth.make_weight_sets(2, hidden, seed=77), hidden, seed=78)
+    eng = LearnedOptimizer(w, hidden, path)
+    shapes = [("w", (64, 96)), ("b", (1000,)), ("odd", (37, 101)), ("tall", (1100, 3))]
+    states = make_states(shapes, recipe="vit", seed=21)
+    for i, st in enumerate(states):
+        st["weight_set"] = i % 2
+    for t in (1, 2):
+        compare_step(eng, states, w, hidden, t, 1.0, tol)
