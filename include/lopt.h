@@ -60,8 +60,9 @@ extern "C" {
 
 /* ---- MLP evaluation paths (lopt_set_mlp_path) -------------------------- */
 #define LOPT_MLP_FP32       0  /* FP32 FMA on CUDA cores (default)          */
-#define LOPT_MLP_TC         1  /* tcgen05 tensor cores, TF32/FP16 operands, */
-                               /* FP32 accumulation                         */
+#define LOPT_MLP_TC         1  /* tcgen05 tensor cores for the two hidden   */
+                               /* layers (FP16 operands, FP32 accumulation);*/
+                               /* output layer in FP32 on CUDA cores        */
 
 typedef struct lopt_ctx* lopt_handle;
 

@@ -11,13 +11,14 @@ import synth
 
 # Tolerances on updated parameters.  Primary: max-norm relative error over
 # the whole updated parameter list, max|got - ref| / max|ref| (1e-5 for the
-# FP32 MLP path, 2e-3 for the tensor-core path: about one unit roundoff of a
-# TF32/BF16 operand).  Secondary, per tensor and element-wise:
+# FP32 MLP path, 2e-3 for the tensor-core path: about one unit roundoff of
+# its FP16 operands, 10-bit mantissa).  Secondary, per tensor and
+# element-wise:
 # |got - ref| / max(|ref|, RMS of ref over the tensor), which is much
 # stricter for tensors whose parameters are all update (zero-initialised
 # biases at step 1): 1e-5 FP32, 1e-2 tensor cores.
 TOL_FP32 = 1e-5      # FP32-FMA MLP path
-TOL_TC = 2e-3        # tensor-core MLP path (TF32 / FP16 operands)
+TOL_TC = 2e-3        # tensor-core MLP path (FP16 operands)
 TOL_ACC = 2e-6       # accumulators m, v, r, c (fp32 EMA vs fp64), element-wise
 TOL_STATS = 2e-5     # per-feature sums of squares, element-wise
 
