@@ -24,6 +24,8 @@ PIN_TESTS = [
     pins.test_p7_indexing_tags,
     lambda: pins.test_p8_weight_decay_alone_is_geometric(0.3, 1e-2),
     pins.test_p8_weight_decay_on_normalised_sgd,
+    pins.test_p9_chunked_sweeps_match_brute_force,
+    pins.test_p10_sampled_path_equals_full_path,
 ]
 
 
@@ -141,7 +143,60 @@ def _mlp_variant(drop_b1=False, drop_b2=False, drop_b3=False, w2_t=False, output
     return mlp
 
 
+def _square_sums_last_chunk_dropped(state, cols, t):
+    n = state["param"].size
+    S = np.zeros(L.N_ELEM_FEATURES)
+    starts = list(range(0, n, L.CHUNK_ELEMENTS))
+    for e0 in starts[:-1] if len(starts) > 1 else starts:
+        idx = np.arange(e0, min(n, e0 + L.CHUNK_ELEMENTS))
+        S += (L._features_of(state, cols, t, idx)[:, :L.N_ELEM_FEATURES] ** 2).sum(axis=0)
+    return S
+
+
+def _square_sums_chunk_overlap(state, cols, t):
+    n = state["param"].size
+    S = np.zeros(L.N_ELEM_FEATURES)
+    for e0 in range(0, n, L.CHUNK_ELEMENTS):
+        idx = np.arange(e0, min(n, e0 + L.CHUNK_ELEMENTS + 1))   # one element counted twice
+        S += (L._features_of(state, cols, t, idx)[:, :L.N_ELEM_FEATURES] ** 2).sum(axis=0)
+    return S
+
+
+_orig_step_tensor = L.step_tensor
+
+
+def _step_tensor_variant(drop_last_update_chunk=False, sampled_unnormalised=False):
+    def step_tensor(state, t, lr, w, sample_idx=None, weight_decay=0.0):
+        R, C = state["shape"]
+        n = R * C
+        if sample_idx is not None and sampled_unnormalised:
+            L.refresh_accumulators(state)
+            S = L.feature_square_sums(state, C, t)
+            F = L._features_of(state, C, t, np.asarray(sample_idx))
+            u = L.update_from_output(L.mlp(F, w))
+            return {"S": S, "sample_param": L.apply_update(state["param"][sample_idx], u, lr, weight_decay),
+                    "sample_update": u}
+        if sample_idx is not None or not drop_last_update_chunk:
+            return _orig_step_tensor(state, t, lr, w, sample_idx=sample_idx, weight_decay=weight_decay)
+        L.refresh_accumulators(state)
+        S = L.feature_square_sums(state, C, t)
+        scales = L.normalisation_scales(S, n)
+        new_p = state["param"].copy()
+        starts = list(range(0, n, L.CHUNK_ELEMENTS))
+        for e0 in starts[:-1] if len(starts) > 1 else starts:
+            idx = np.arange(e0, min(n, e0 + L.CHUNK_ELEMENTS))
+            o = L.mlp(L.normalise(L._features_of(state, C, t, idx), scales), w)
+            new_p[idx] = L.apply_update(state["param"][idx], L.update_from_output(o), lr, weight_decay)
+        state["param"] = new_p
+        return {"S": S, "scales": scales, "rho": list(state["rho"])}
+    return step_tensor
+
+
 MUTATIONS = {
+    "square sums: last chunk dropped": ("feature_square_sums", _square_sums_last_chunk_dropped),
+    "square sums: chunks overlap by one element": ("feature_square_sums", _square_sums_chunk_overlap),
+    "update loop: last chunk dropped": ("step_tensor", _step_tensor_variant(drop_last_update_chunk=True)),
+    "sampled path: features left unnormalised": ("step_tensor", _step_tensor_variant(sampled_unnormalised=True)),
     "epsilon 1e-8": ("EPS", 1e-8),
     "time scales reversed": ("TIME_SCALES", tuple(reversed(L.TIME_SCALES))),
     "v an EMA of |g|": ("accumulator_update", _v_of_abs_g),

@@ -417,3 +417,76 @@ def test_p8_zero_decay_is_the_plain_step():
     O.step_tensor(a, 2, 0.5, w)
     O.step_tensor(b, 2, 0.5, w, weight_decay=0.0)
     assert np.array_equal(a["param"], b["param"])
+
+
+# ---------------------------------------------------------------------------
+# P9: the chunked sweeps (feature sums and the update loop run over element
+# chunks only to bound host memory) against the scalar brute force
+# ---------------------------------------------------------------------------
+def test_p9_chunked_sweeps_match_brute_force():
+    """Chunks of 5 elements over a 7 x 9 tensor: 13 chunks, the last one
+    ragged (3 elements), and chunk edges that cut rows.  A dropped or
+    shifted chunk changes the square sums of every feature and leaves
+    elements without their update, so the brute force disagrees."""
+    import oracle.lopt_oracle as L
+    saved = L.CHUNK_ELEMENTS
+    L.CHUNK_ELEMENTS = 5
+    try:
+        _p9_body()
+    finally:
+        L.CHUNK_ELEMENTS = saved
+
+
+def _p9_body():
+    rng = np.random.default_rng(21)
+    R, C, H = 7, 9, 4
+    n = R * C
+    W = rng.normal(size=O.weight_set_size(H)) * 0.6
+    p = list(rng.normal(size=n) * 0.02)
+    bf = {"m": [[0.0] * n for _ in range(3)], "v": [0.0] * n,
+          "r": [[0.0] * R for _ in range(3)], "c": [[0.0] * C for _ in range(3)]}
+    st = O.new_state((R, C), np.array(p), np.zeros(n))
+    w = O.unpack_weights(W, H)
+    for t in (1, 2):
+        g = list(rng.normal(size=n) * 1e-3)
+        st["grad"] = np.array(g)
+        p_old = st["param"].copy()
+        out = O.step_tensor(st, t, 0.9, w)
+        p = brute_force_step(R, C, p, g, bf, t, 0.9, list(W), H)
+        np.testing.assert_allclose(st["param"], p, rtol=1e-12, atol=1e-300)
+        # the square sums over all chunks equal one sum over the whole tensor
+        # (features of the refreshed accumulators and the pre-step parameters)
+        F = O.features(p_old, st["grad"], st["mom"], st["rms"], st["row"], st["col"],
+                       st["rho"], C, t)
+        np.testing.assert_allclose(out["S"], (F[:, :28] ** 2).sum(axis=0), rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# P10: the sampled path (updates at chosen elements only, used for the
+# full-size checks) equals the full step at the same elements
+# ---------------------------------------------------------------------------
+def test_p10_sampled_path_equals_full_path():
+    rng = np.random.default_rng(22)
+    R, C, H = 6, 11, 8
+    n = R * C
+    W = O.unpack_weights(rng.normal(size=O.weight_set_size(H)) * 0.5, H)
+    p = rng.normal(size=n) * 0.02
+    m = [rng.normal(size=n) * 1e-3 for _ in range(3)]
+    v = rng.random(n) * 1e-6
+    row = [rng.random(R) * 1e-6 for _ in range(3)]
+    col = [rng.random(C) * 1e-6 for _ in range(3)]
+    g = rng.normal(size=n) * 1e-3
+    idx = np.array([0, 5, 11, 12, 37, 40, n - 1])
+    full = O.new_state((R, C), p, g, m, v, row, col)
+    samp = O.new_state((R, C), p, g, m, v, row, col)
+    O.step_tensor(full, 4, 0.8, W, weight_decay=0.01)
+    out = O.step_tensor(samp, 4, 0.8, W, sample_idx=idx, weight_decay=0.01)
+    np.testing.assert_allclose(out["sample_param"], full["param"][idx], rtol=1e-15, atol=1e-300)
+    # the update itself: p_old - p_new = lr * (u + wd * p_old)
+    np.testing.assert_allclose(0.8 * (out["sample_update"] + 0.01 * p[idx]),
+                               p[idx] - full["param"][idx], rtol=1e-12, atol=1e-300)
+    # the sampled call leaves the parameters alone but refreshes the accumulators
+    np.testing.assert_array_equal(samp["param"], p)
+    for k in range(3):
+        np.testing.assert_array_equal(samp["mom"][k], full["mom"][k])
+        np.testing.assert_array_equal(samp["col"][k], full["col"][k])
