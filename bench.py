@@ -37,9 +37,6 @@ UNIT = "params/s"
 # Learned Optimizers in PyTorch", section "ステップ時間の削減": 99.59 ms,
 # hardware not stated): 86,415,592 params / 0.09959 s.
 PAGE_VIT_PARAMS_PER_S = 86415592 / 0.09959
-# rough single-thread speed of the fp64 oracle on a server core, used only to
-# size the reference arm's per-step sample
-ORACLE_PARAMS_PER_S = 1.2e6
 FP32_LANES_PER_SM = 128
 
 
@@ -52,140 +49,197 @@ def parse():
     ap.add_argument("--workload", default="vit_b16")
     ap.add_argument("--mlp", default="auto", choices=["auto", "tc", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-elems", type=int, default=6_000_000)
+    ap.add_argument("--cpu-sample-elems", type=int, default=100_000_000)
     return ap.parse_args()
 
 
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reported baseline; never the product path)
 # ---------------------------------------------------------------------------
-def _oracle_sample_shapes(wl, max_elems):
-    """Leading tensors of the workload, up to about max_elems parameters.  A
-    leading matrix larger than the whole budget is cut to its first rows."""
-    out, n = [], 0
-    for name, shape in wl.shapes:
-        k = 1
-        for s in shape:
-            k *= s
-        if not out and k > max_elems and len(shape) >= 2:
-            shape = (max(1, max_elems // shape[-1]),) + tuple(shape[1:])
-            name, k = name + "[leading rows]", shape[0] * shape[-1]
-        if out and n + k > max_elems:
-            continue
-        out.append((name, shape))
-        n += k
-        if n >= max_elems:
-            break
-    return out, n
+def _single_thread_env():
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"
+    os.environ["CUDA_VISIBLE_DEVICES"] = ""
 
 
-def oracle_worker(workload: str, max_elems: int, steps: int) -> dict:
-    """Runs in a fresh single-threaded process: times oracle steps over a
-    bounded sample of the workload (inputs drawn by the same generators)."""
-    import numpy as np
+def _pool_init(root):
+    _single_thread_env()
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import torch
+    torch.set_num_threads(1)
+
+
+def _pool_step(job):
+    """One worker task: draw tensor ``ti`` of the workload (the same
+    generators as the whole list) and time ``steps`` oracle steps on it."""
+    workload, ti, steps = job
     import oracle as O
     import synth
     wl = synth.workloads()[workload]
-    shapes, n = _oracle_sample_shapes(wl, max_elems)
-    states = synth.make_list(wl, "cpu", seed=0, shapes=shapes)
-    w = synth.make_weight_sets(len(shapes) if wl.per_tensor_weights else 1, wl.hidden)
-    ws = [O.unpack_weights(x, wl.hidden) for x in w]
-    ost = [O.new_state((s["rows"], s["cols"]), s["param"].numpy(), s["grad"].numpy(),
-                       mom=[m.numpy() for m in s["mom"]], rms=s["rms"].numpy(),
-                       row=[r.numpy() for r in s["row"]], col=[c.numpy() for c in s["col"]],
-                       weight_set=s["weight_set"]) for s in states]
-    times = []
+    s = synth.make_list(wl, "cpu", seed=0, indices={ti})[0]
+    w = synth.make_weight_sets(1, wl.hidden, seed=1234 + (ti if wl.per_tensor_weights else 0))
+    st = O.new_state((s["rows"], s["cols"]), s["param"].numpy(), s["grad"].numpy(),
+                     mom=[m.numpy() for m in s["mom"]], rms=s["rms"].numpy(),
+                     row=[r.numpy() for r in s["row"]], col=[c.numpy() for c in s["col"]])
+    wu = O.unpack_weights(w[0], wl.hidden)
+    t0 = time.perf_counter()
     for k in range(steps):
+        O.step_tensor(st, wl.first_step + k, 1.0, wu)
+    return s["rows"] * s["cols"], time.perf_counter() - t0
+
+
+def _cpu_model():
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            if ln.startswith("Model name:"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform_machine()
+
+
+def platform_machine():
+    import platform
+    return platform.machine()
+
+
+def oracle_pool(workload: str, tensor_ids, steps: int, cores: int) -> dict:
+    """The fp64 oracle over the given tensors of the workload on ``cores``
+    host cores: a process pool (spawn start, one single-threaded worker per
+    core) that steps whole tensors, largest first.  Returns the wall time of
+    the whole set of tensors (after the workers have started)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    import synth
+    wl = synth.workloads()[workload]
+    size = lambda ti: synth.numel(wl.shapes[ti][1])
+    order = sorted(tensor_ids, key=size, reverse=True)
+    with ctx.Pool(cores, initializer=_pool_init, initargs=(ROOT,)) as pool:
+        pool.map(_pool_step, [(workload, order[-1], 1)] * cores)   # start every worker
         t0 = time.perf_counter()
-        for st in ost:
-            O.step_tensor(st, wl.first_step + k, 1.0, ws[st["weight_set"]])
-        times.append(time.perf_counter() - t0)
-    return {"elements": n, "tensors": len(shapes), "step_s": times}
-
-
-def run_oracle_subprocess(workload: str, max_elems: int, steps: int) -> dict:
-    env = dict(os.environ)
-    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[v] = "1"
-    env["CUDA_VISIBLE_DEVICES"] = ""
-    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
-            "print(json.dumps(bench.oracle_worker(%r, %d, %d)))" % (ROOT, workload, max_elems, steps))
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       cwd=ROOT, timeout=1800)
-    if r.returncode != 0:
-        raise RuntimeError("oracle subprocess failed: " + r.stderr[-2000:])
-    return json.loads(r.stdout.strip().splitlines()[-1])
+        res = pool.map(_pool_step, [(workload, ti, steps) for ti in order], chunksize=1)
+        wall = time.perf_counter() - t0
+    n = sum(r[0] for r in res)
+    return {"elements": n, "tensors": len(order), "wall_s": wall, "steps": steps,
+            "cpu_s": sum(r[1] for r in res)}
 
 
 def cpu_baseline(workload: str, max_elems: int) -> dict:
-    res = run_oracle_subprocess(workload, max_elems, 1)
-    s = res["step_s"][0]
-    return {"value": res["elements"] / s, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "%d leading tensors (%d params) of %s, one step, fp64 numpy, 1 thread"
-                      % (res["tensors"], res["elements"], workload),
-            "seconds": s}
+    """The oracle as it stands on every host core, one step over whole
+    tensors of the workload: every tensor when the list has at most
+    ``max_elems`` parameters, else the largest tensors first up to that many."""
+    import synth
+    wl = synth.workloads()[workload]
+    sizes = [(synth.numel(s), ti) for ti, (_, s) in enumerate(wl.shapes)]
+    ids, n = [], 0
+    for k, ti in sorted(sizes, key=lambda x: x[1]):
+        if n + k > max_elems and ids:
+            continue
+        ids.append(ti)
+        n += k
+    cores = min(os.cpu_count() or 1, len(ids))
+    res = oracle_pool(workload, ids, 1, cores)
+    total = sum(k for k, _ in sizes)
+    return {"value": res["elements"] / res["wall_s"], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of %d tensors (%d of %d params, %.0f%%) of %s, one step, fp64 numpy oracle, "
+                      "process pool of %d single-threaded workers (%s)"
+                      % (res["tensors"], len(wl.shapes), res["elements"], total,
+                         100.0 * res["elements"] / total, workload, cores, _cpu_model()),
+            "seconds": res["wall_s"]}
 
 
 # ---------------------------------------------------------------------------
 # Clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons of one GPU, sampled every few
+    milliseconds by a thread of this process through NVML's read-only
+    queries (libnvidia-ml through ctypes); ``leg(name)`` labels the samples
+    taken from then on.  Falls back to no samples when NVML is missing."""
+    NVML_CLOCK_SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, gpu_index: int):
-        self.idx = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, pci_bus_id=None, index=0, period_s=0.005):
+        import ctypes
+        self.samples = []          # (leg, sm_mhz, power_w, reasons bitmask)
+        self.period = period_s
+        self.cur = "idle"
+        self.max_mhz = None
+        self.h = None
+        self.error = None
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            h = ctypes.c_void_p()
+            rc = -1
+            if pci_bus_id:
+                rc = self.nv.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h))
+            if rc != 0:
+                rc = self.nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h))
+            if rc != 0:
+                raise RuntimeError("no NVML handle")
+            self.h = h
+            mx = ctypes.c_uint()
+            if self.nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+        except Exception as e:   # no NVML: the line reports no samples
+            self.error = str(e)
+            self.h = None
+
+    def _one(self):
+        import ctypes
+        mhz, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(mhz)) != 0:
+            return
+        self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw))
+        if self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs)) != 0:
+            self.nv.nvmlDeviceGetCurrentClocksThrottleReasons(self.h, ctypes.byref(rs))
+        self.samples.append((self.cur, float(mhz.value), mw.value / 1e3, int(rs.value)))
+
+    def _run(self):
+        while not self.stop_flag:
+            self._one()
+            time.sleep(self.period)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+        self.stop_flag = False
+        if self.h is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
             self.thread.start()
-            t0 = time.time()
-            while not self.lines and time.time() - t0 < 3.0 and self.proc.poll() is None:
-                time.sleep(0.02)
-            self.lines.clear()
-        except Exception:
-            self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def leg(self, name):
+        self.cur = name
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except Exception:
-                self.proc.kill()
+        self.stop_flag = True
+        if self.h is not None:
+            self.thread.join(timeout=2)
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
-            except ValueError:
-                continue
-            for nm, v in zip(names, f[5:9]):
-                if v.lower() == "active":
+    def summary(self, legs=("timed", "e2e")):
+        """Median SM clock over the samples of the given legs, the reasons
+        seen there, and the sample count per leg."""
+        per_leg = {}
+        for lg, *_ in self.samples:
+            per_leg[lg] = per_leg.get(lg, 0) + 1
+        sel = [s for s in self.samples if s[0] in legs]
+        reasons = set()
+        for _, _, _, rs in sel:
+            for bit, nm in self.REASONS.items():
+                if rs & bit:
                     reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "samples_per_leg": per_leg, "source": "nvml" if self.h is not None else
+                    "none (%s)" % self.error}
+        return {"sm_mhz": statistics.median(s[1] for s in sel), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(sel), "samples_per_leg": per_leg,
+                "power_w_max": max(s[2] for s in sel), "period_ms": self.period * 1e3,
+                "source": "nvml, in-process thread"}
 
 
 # ---------------------------------------------------------------------------
@@ -330,6 +384,14 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     props = torch.cuda.get_device_properties(dev)
 
+    pci = None
+    try:
+        pci = "%04x:%02x:%02x.0" % (props.pci_domain_id, props.pci_bus_id, props.pci_device_id)
+    except AttributeError:
+        pass
+    clk = ClockSampler(pci, local_rank)
+    clk.__enter__()
+    clk.leg("warmup")
     t = wl.first_step
     for _ in range(args.warmup):
         eng.step(prepared, t, 1.0, stream)
@@ -346,13 +408,14 @@ def run_ours(args, rank, world, local_rank):
     eng.kernel_times()
     barrier()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local_rank) as clk:
-        start.record(stream)
-        for _ in range(args.steps):
-            eng.step(prepared, t, 1.0, stream)
-            t += 1
-        stop.record(stream)
-        barrier()
+    clk.leg("timed")
+    start.record(stream)
+    for _ in range(args.steps):
+        eng.step(prepared, t, 1.0, stream)
+        t += 1
+    stop.record(stream)
+    barrier()
+    clk.leg("idle")
     eng.check()
     ms_total = max_over_ranks(start.elapsed_time(stop), world, dev)
     kms, klaunch = eng.kernel_times()
@@ -375,6 +438,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_steps = max(3, args.steps // 2)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk.leg("e2e")
     e0.record(stream)
     for _ in range(e2e_steps):
         eng.step_host(prepared, g_host, p_host, t, 1.0, stream)
@@ -382,6 +446,8 @@ def run_ours(args, rank, world, local_rank):
     eng.host_sync(stream)   # the last parameters are in host memory
     e1.record(stream)
     barrier()
+    clk.leg("idle")
+    clk.__exit__()
     eng.check()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     e2e_value = job_throughput(numel, world, e2e_steps, e2e_ms)
@@ -445,19 +511,40 @@ def run_ours(args, rank, world, local_rank):
 
 
 def run_reference(args, rank):
-    """The CPU oracle timed on this host on a bounded sample per step."""
+    """The CPU oracle, as it stands, timed on this host's cores: each step is
+    one oracle step over a bounded sample of whole tensors of the workload
+    (the same sample every step), spread over a process pool."""
     if rank != 0:
         return None
     import synth
     wl = synth.workloads()[args.workload]
-    # a bounded sample per step: the whole run stays near two minutes
-    per_step = int(min(1_000_000, max(65_536, 120 * ORACLE_PARAMS_PER_S / (args.warmup + args.steps))))
-    res = run_oracle_subprocess(args.workload, per_step, args.warmup + args.steps)
-    times = res["step_s"][args.warmup:]
+    cores = os.cpu_count() or 1
+    # about 0.5 M params per core per step: the whole run stays within minutes
+    budget = 500_000 * cores
+    ids, n = [], 0
+    for ti, (_, s) in enumerate(wl.shapes):
+        k = synth.numel(s)
+        if n + k > budget and ids:
+            continue
+        ids.append(ti)
+        n += k
+    cores = min(cores, len(ids))
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    times = []
+    with ctx.Pool(cores, initializer=_pool_init, initargs=(ROOT,)) as pool:
+        pool.map(_pool_step, [(args.workload, ids[0], 1)] * cores)   # start every worker
+        order = sorted(ids, key=lambda ti: synth.numel(wl.shapes[ti][1]), reverse=True)
+        for _ in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            pool.map(_pool_step, [(args.workload, ti, 1) for ti in order], chunksize=1)
+            times.append(time.perf_counter() - t0)
+    times = times[args.warmup:]
     tot = sum(times)
-    value = res["elements"] * len(times) / tot
-    sample = ("%d leading tensors (%d params) of %s per step, fp64 numpy oracle, 1 thread"
-              % (res["tensors"], res["elements"], args.workload))
+    value = n * len(times) / tot
+    sample = ("%d of %d tensors (%d params) of %s per step, fp64 numpy oracle, process pool of %d "
+              "single-threaded workers (%s); wall time per step includes each tensor's input draw"
+              % (len(ids), len(wl.shapes), n, args.workload, cores, _cpu_model()))
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot / len(times) * 1e3,
@@ -465,7 +552,7 @@ def run_reference(args, rank):
         "data": "synthetic",
         "config": {"workload": "%s (%d tensors in the full list)" % (args.workload, len(wl.shapes)),
                    "sample": sample},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

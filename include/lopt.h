@@ -123,10 +123,15 @@ int lopt_create(const float* mlp_weights, int d_feat, int hidden, int n_sets,
 
 /*
  * Choose how the MLP is evaluated by later lopt_step() calls:
- * LOPT_MLP_FP32 (exact FP32 arithmetic) or LOPT_MLP_TC (tensor cores: FP16
- * operands for the first two layers with FP32 accumulation, output layer in
- * FP32; about 1e-3 relative error on the update).  LOPT_E_UNSUPPORTED if the
- * path cannot run this handle's hidden width.
+ * LOPT_MLP_FP32 (exact FP32 arithmetic) or LOPT_MLP_TC (tensor cores for
+ * the two hidden layers: the 28 normalised features, W1, b1 + sum_s tau_s
+ * W1[28 + s], ReLU(h1) and W2 in FP16 with FP32 accumulation, b2 in FP32;
+ * the output layer in FP32 on CUDA cores).  The FP16 operands cost about
+ * 1e-3 of the update's RMS on average and up to a few 1e-2 of it on outlier
+ * elements (as an exact FP16-operand MLP does); an updated parameter of a
+ * tensor that is not all update (weights, LayerNorm scales) stays within
+ * 2e-3 of the exact value.  LOPT_E_UNSUPPORTED if the path cannot run this
+ * handle's hidden width (it covers widths up to 32).
  */
 int lopt_set_mlp_path(lopt_handle h, int path);
 
@@ -298,10 +303,15 @@ int lopt_kernel_times(lopt_handle h, double* ms, int64_t* launches);
  * framework that owns every device allocation, or under a fixed device-memory
  * budget, or on a path where cudaMalloc's implicit device-wide
  * synchronisation is not acceptable.  It runs the same row/column kernel as
- * lopt_step() (same strips, same summation order) but takes its scratch from
- * a fixed array of LOPT_STATIC_SCRATCH_BYTES bytes that the library reserves
- * in device memory of every GPU on which it is loaded, held until the process
- * exits.  No handle is needed.
+ * lopt_step() over the same strips, but takes its scratch from a fixed array
+ * of LOPT_STATIC_SCRATCH_BYTES bytes that the library reserves in device
+ * memory of every GPU on which it is loaded, held until the process exits.
+ * When grad, the column accumulators and every other array lopt_step() is
+ * given for the tensor are 16-byte aligned (as torch allocations are), both
+ * calls take the same 128-bit route and their results are the same bits;
+ * otherwise they agree to rounding.  The descriptor and unit table are
+ * written into the scratch by a small kernel from its launch parameters (no
+ * host-to-device copy).  No handle is needed.
  *   grad     DEVICE [rows*cols] fp32, read.
  *   row      HOST array of 3 DEVICE pointers, [rows] fp32 each: the row
  *            accumulators (decays 0.1, 0.5, 0.9), updated in place.

@@ -387,9 +387,10 @@ void* g_scratch_addr[kMaxScratchDevices] = {};
 // is looked up once per device, with that device current, and cached.
 int scratch_address(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) {
     cudaGetLastError();
-    return LOPT_E_CUDA;
+    return record_cuda_error(ge);
   }
   if (dev < 0 || dev >= kMaxScratchDevices) return LOPT_E_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
@@ -398,7 +399,7 @@ int scratch_address(void** out) {
     const cudaError_t e = cudaGetSymbolAddress(&p, g_rowcol_scratch);
     if (e != cudaSuccess || !p) {
       cudaGetLastError();
-      return LOPT_E_CUDA;
+      return record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol);
     }
     g_scratch_addr[dev] = p;
   }
@@ -407,6 +408,16 @@ int scratch_address(void** out) {
 }
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Fills the scratch for one call from the kernel's parameters: the tensor's
+// descriptor, its unit table (one unit per strip) and the zeroed counter
+// and status words.  No host memory is involved.
+__global__ void k_static_setup(TensorDesc d, TensorDesc* desc, Unit* units, int n_strips, int32_t* words) {
+  const int tid = threadIdx.x;
+  if (tid == 0) *desc = d;
+  if (tid < 64) words[tid] = 0;
+  for (int s = tid; s < n_strips; s += blockDim.x) units[s] = Unit{0, s};
+}
 
 }  // namespace
 }  // namespace lopt
@@ -432,7 +443,8 @@ extern "C" int lopt_rowcol_static(const float* grad, float* const* row, float* c
   for (size_t k = 1; k < spans.size(); ++k)
     if (spans[k].lo < spans[k - 1].hi) return LOPT_E_ALIAS;
 
-  // Same decomposition as lopt_step(), so the results are the same bits.
+  // Same strips as lopt_step(); with 16-byte aligned arrays both take the
+  // 128-bit route, and then the results are the same bits.
   const int strip_rows = strip_rows_for(rows, cols);
   const int n_strips = (int)((rows + strip_rows - 1) / strip_rows);
   const size_t o_desc = 0;
@@ -467,16 +479,13 @@ extern "C" int lopt_rowcol_static(const float* grad, float* const* row, float* c
   d.n_strips = n_strips;
   d.colpart_off = 0;
   d.rowpart_off = 0;
-  std::vector<Unit> units((size_t)n_strips);
-  for (int s = 0; s < n_strips; ++s) units[(size_t)s] = {0, s};
-
-  // Pageable sources are staged by the runtime before these calls return.
-  cudaError_t e = cudaMemcpyAsync(sc + o_desc, &d, sizeof(d), cudaMemcpyHostToDevice, stream);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(sc + o_units, units.data(), sizeof(Unit) * units.size(),
-                        cudaMemcpyHostToDevice, stream);
-  // The last-block counter and the status word must start at zero.
-  if (e == cudaSuccess) e = cudaMemsetAsync(sc + o_cnt, 0, 256, stream);
+  cudaError_t e = cudaSuccess;
+  {
+    k_static_setup<<<1, 256, 0, stream>>>(d, reinterpret_cast<TensorDesc*>(sc + o_desc),
+                                          reinterpret_cast<Unit*>(sc + o_units), n_strips,
+                                          reinterpret_cast<int32_t*>(sc + o_cnt));
+    e = cudaGetLastError();
+  }
   if (e == cudaSuccess) {
     StepArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -495,7 +504,7 @@ extern "C" int lopt_rowcol_static(const float* grad, float* const* row, float* c
                         cudaMemcpyDeviceToDevice, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
-    return LOPT_E_CUDA;
+    return record_cuda_error(e);
   }
   return LOPT_OK;
 }

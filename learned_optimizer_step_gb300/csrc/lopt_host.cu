@@ -25,6 +25,17 @@
 namespace lopt {
 bool apply_fp32_supported(int hidden);
 
+namespace {
+// The last CUDA error a call of this thread failed on (lopt_last_cuda_error).
+thread_local std::string g_last_cuda;
+}  // namespace
+
+int record_cuda_error(cudaError_t e) {
+  g_last_cuda = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
+  if (e == cudaErrorMemoryAllocation) return LOPT_E_OOM;
+  return LOPT_E_CUDA;
+}
+
 // Rows per K0 strip.  About kStripTarget elements per strip, but no more
 // than kFinalizeCap / cols strips (the last block of a tensor sums
 // strips x cols column partials) and no more than kMaxStripRows rows.
@@ -93,14 +104,7 @@ struct lopt_ctx {
 
 namespace {
 
-// The last CUDA error a call of this thread failed on (lopt_last_cuda_error).
-thread_local std::string g_last_cuda;
-
-int cuda_fail(cudaError_t e) {
-  g_last_cuda = std::string(cudaGetErrorName(e)) + ": " + cudaGetErrorString(e);
-  if (e == cudaErrorMemoryAllocation) return LOPT_E_OOM;
-  return LOPT_E_CUDA;
-}
+int cuda_fail(cudaError_t e) { return lopt::record_cuda_error(e); }
 
 int padded_hidden(int h) {
   for (int c : {4, 8, 16, 32, 64})

@@ -240,6 +240,10 @@ __host__ __device__ inline int w_set_size(int H) { return kDFeat * H + 4 * H + H
 // Status flags written by kernels.
 enum : int32_t { kStatusTimeout = 1 };
 
+// Records a CUDA error for lopt_last_cuda_error() (this host thread) and
+// returns the matching library code (LOPT_E_OOM or LOPT_E_CUDA).
+int record_cuda_error(cudaError_t e);
+
 // ---- launchers (one per kernel file) ---------------------------------------
 cudaError_t launch_rowcol(const StepArgs& a, cudaStream_t s);
 int  strip_rows_for(int64_t R, int64_t C);   // K0 rows per strip of an [R x C] tensor

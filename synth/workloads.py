@@ -211,12 +211,16 @@ def make_weight_sets(n_sets: int, hidden: int, seed: int = 1234,
     return out
 
 
-def make_list(wl: Workload, device, seed: int = 0, shapes=None) -> List[dict]:
+def make_list(wl: Workload, device, seed: int = 0, shapes=None, indices=None) -> List[dict]:
     """Initial state for every tensor of a workload (torch tensors on
-    ``device``): param, grad (step ``wl.first_step``), accumulators."""
+    ``device``): param, grad (step ``wl.first_step``), accumulators.
+    ``indices``: only these tensors of the list, drawn exactly as in the
+    whole list."""
     shapes = wl.shapes if shapes is None else shapes
     out = []
     for ti, (name, shape) in enumerate(shapes):
+        if indices is not None and ti not in indices:
+            continue
         R, C = rows_cols(shape)
         s = seed + 7919 * ti
         st = {"name": name, "shape": tuple(shape), "rows": R, "cols": C,

@@ -14,7 +14,8 @@ import pytest
 
 import oracle as O
 import synth
-from tests.gpu_helpers import TOL_FP32, TOL_TC, cpu, elem_tol, need_gpu, rel_err, to_oracle
+from tests import tc_emulation as E
+from tests.gpu_helpers import TOL_FP32, TOL_TC, check_param, cpu, need_gpu, rel_err, to_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -59,9 +60,13 @@ def _oracle(workload, states):
         for i in _subset(states):
             st = states[i]
             r = to_oracle(st)
+            e = to_oracle(st)
             sidx = _samples(st)
+            p_old = r["param"][sidx].copy()
             res = O.step_tensor(r, wl.first_step, 1.0, ws[st["weight_set"]], sample_idx=sidx)
-            out[i] = {"sidx": sidx, "param": res["sample_param"], "S": res["S"],
+            emu = E.step_tensor(e, wl.first_step, 1.0, ws[st["weight_set"]], sample_idx=sidx, S=res["S"])
+            out[i] = {"sidx": sidx, "param": res["sample_param"], "S": res["S"], "p_old": p_old,
+                      "emu": emu["sample_param"],
                       "col0": r["col"][0].copy(), "mom1_sample": r["mom"][1][sidx].copy()}
         _ORACLE[workload] = out
     return _ORACLE[workload]
@@ -79,17 +84,13 @@ def _run(workload, path, tol):
     eng.step(states, wl.first_step, 1.0)
     eng.check()
     torch.cuda.synchronize()
-    num = den = 0.0
     for i, r in ref.items():
         st = states[i]
         got = cpu(st["param"])[r["sidx"]]
-        num = max(num, float(np.max(np.abs(got - r["param"]))))
-        den = max(den, float(np.max(np.abs(r["param"]))))
-        assert rel_err(got, r["param"]) <= elem_tol(tol), (st["name"], rel_err(got, r["param"]))
+        check_param(st["name"], tol, r["p_old"], got, r["param"], r["emu"] if tol > TOL_FP32 else None)
         assert rel_err(eng.feature_stats(i), r["S"], floor=1e-300) <= 2e-5, st["name"]
         assert rel_err(cpu(st["col"][0]), r["col0"]) <= 2e-6, st["name"]
         assert rel_err(cpu(st["mom"][1])[r["sidx"]], r["mom1_sample"]) <= 2e-6, st["name"]
-    assert num / den <= tol, num / den
     eng.close()
     del states
     torch.cuda.empty_cache()

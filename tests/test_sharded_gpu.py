@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from tests.gpu_helpers import (TOL_FP32, TOL_TC, cpu, elem_tol, make_states, need_gpu, rel_err,
+from tests.gpu_helpers import (TOL_FP32, TOL_TC, check_param, cpu, make_states, need_gpu, rel_err,
                                to_oracle)
 
 pytestmark = pytest.mark.gpu
@@ -66,13 +66,11 @@ def test_two_simulated_ranks_match_oracle(path, tol):
     e1.check()
     torch.cuda.synchronize()
     ws = O.unpack_weights(w[0], 32)
-    num = den = 0.0
     for ti, r in enumerate(ref):
+        p_old = r["param"].copy()
         out = O.step_tensor(r, 2, 0.9, ws)
         got = np.concatenate([cpu(ranks[0][ti]["param"]), cpu(ranks[1][ti]["param"])])
-        num = max(num, float(np.max(np.abs(got - r["param"]))))
-        den = max(den, float(np.max(np.abs(r["param"]))))
-        assert rel_err(got, r["param"]) <= elem_tol(tol), (SHAPES[ti], rel_err(got, r["param"]))
+        check_param(str(SHAPES[ti]), tol, p_old, got, r["param"])
         for k in range(3):
             for rk in ranks:
                 assert rel_err(cpu(rk[ti]["col"][k]), r["col"][k]) <= 2e-6
@@ -82,7 +80,6 @@ def test_two_simulated_ranks_match_oracle(path, tol):
         assert rel_err(S, out["S"], floor=1e-300) <= 2e-5, SHAPES[ti]
         got_m = np.concatenate([cpu(ranks[0][ti]["mom"][2]), cpu(ranks[1][ti]["mom"][2])])
         assert rel_err(got_m, r["mom"][2]) <= 2e-6
-    assert num / den <= tol
 
 
 @pytest.mark.parametrize("path", ["fp32", "tc"])

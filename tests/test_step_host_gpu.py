@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle as O
-from tests.gpu_helpers import TOL_FP32, TOL_TC, cpu, elem_tol, make_states, need_gpu, rel_err, to_oracle
+from tests.gpu_helpers import TOL_FP32, TOL_TC, check_param, cpu, make_states, need_gpu, rel_err, to_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -123,14 +123,11 @@ def test_host_step_matches_oracle(path, tol):
     eng.check()
     torch.cuda.synchronize()
     ws = O.unpack_weights(w[0], 32)
-    num = den = 0.0
     for i, r in enumerate(ref):
+        p_old = r["param"].copy()
         O.step_tensor(r, 4, 0.7, ws)
         got = p_host[i].numpy().astype(np.float64)
-        assert rel_err(got, r["param"]) <= elem_tol(tol), SMALL[i]
-        num = max(num, float(np.max(np.abs(got - r["param"]))))
-        den = max(den, float(np.max(np.abs(r["param"]))))
-    assert num / den <= tol
+        check_param(str(SMALL[i]), tol, p_old, got, r["param"])
 
 
 def test_host_step_weight_decay_and_path_follow_the_handle():
