@@ -12,17 +12,18 @@
 //   warp 16      producer: bulk-copies (cp.async.bulk, one array per lane) p,
 //                g, m0..2, v of up to 8 tiles (a stage) of a work unit into a
 //                ring of shared-memory stages, and writes p, m0..2, v of a
-//                stage back with bulk copies once its two owners are done;
+//                stage back with bulk copies once its feature group is done;
 //   warps 8-15   two feature warpgroups, owning alternate stages: EMA
 //                update, features, normalisation, FP16 A operand of layer 1
-//                into the tile slot's tensor memory; the updated m and v go
-//                back into the stage;
+//                into the tile slot's tensor memory (the updated m and v go
+//                back into the stage); then, for the same tiles, once their
+//                layer-2 result is in: ReLU(h2), the two-unit output layer
+//                in FP32 on the CUDA cores, and the update of p in the stage
+//                (lane t of a stage's tiles holds the thread's own elements);
 //   warps 17-18  MMA issuers, one thread each: layer 1 and layer 2;
 //   warps 0-7    two epilogue warpgroups, owning alternate stages, two
 //                tiles at a time: ReLU + FP16 A operand of layer 2 (in
-//                tensor memory) and the b2 preset of its accumulator; then
-//                ReLU(h2), the two-unit output layer in FP32 on the CUDA
-//                cores, and the update of p in the stage.
+//                tensor memory) and the b2 preset of its accumulator.
 // A tile is 128 elements of one tensor (one per TMEM lane); four tiles
 // cover 512 consecutive elements, lane t of each holding one of elements
 // 4t..4t+3, so that a feature thread finds the row of four consecutive
@@ -34,20 +35,21 @@
 // small record, so the feature warps keep no per-tensor state.  Owning whole
 // stages keeps the per-tile control flow of the warps small.
 //
-// Small MMAs (M=128, N<=32) cost about 50 cycles of the SM's MMA pipe each,
-// whatever their K, and a few hundred cycles pass from issue to a waiting
-// thread.  So a tile uses few MMAs (FP16 operands, K = 32 for layer 1 with b1
+// A small MMA (M=128, N<=32) keeps its issuing thread about 120 cycles,
+// whatever its N (measured: 122-162 cycles for N from 16 to 256), and about
+// 130 cycles more pass from its commit to a waiting thread.  So a tile uses few MMAs (FP16 operands, K = 32 for layer 1 with b1
 // against a constant 1 in the A operand, K = NP for layer 2 onto the preset
 // b2: 4 MMAs at NP = 32, one tcgen05.commit per layer and tile) and only two
 // MMA round trips: the output layer (two units) runs on the CUDA cores.  The
-// two layers are issued by two threads in different warps, so that issuing
-// (a few dozen instructions per tile) is spread over two schedulers.  At
+// two layers are issued by two threads in different warps, which issue side
+// by side.  At
 // most S tiles are in flight (10 slots at NP = 32), and a tile keeps its
 // slot from its features to the read of its layer-2 result, so S tiles per
-// slot lifetime bound the throughput.  Most of that lifetime is the wait
-// for an epilogue group; hence the epilogue's two tiles at a time (shared
-// reads of b2 and W3), and hence no third MMA for the output layer: its
-// round trip lengthens the lifetime more than it shortens the epilogue.
+// slot lifetime bound the throughput.  Much of that lifetime is the wait for
+// an epilogue group; hence the epilogue's two tiles at a time (shared reads
+// of b2), the second half of each tile's epilogue in the feature groups
+// (which have slack), and no third MMA for the output layer: its round trip
+// lengthens the lifetime more than it shortens the epilogue.
 //
 // The tiles of a CTA are processed in sessions: maximal runs of tiles whose
 // tensors share one MLP weight set.  Between sessions the pipeline drains,
@@ -81,7 +83,7 @@ constexpr int kStageElems = kStageTiles * kTile;
 constexpr int kArrays = 6;                // p, g, m0, m1, m2, v
 constexpr int kRingStages = 6;            // stages held in shared memory
 constexpr int kStageBytes = kArrays * kStageElems * 4;
-constexpr int kStageUsers = 2 * kTile;    // the feature and the epilogue group that own a stage
+constexpr int kStageUsers = kTile;        // the feature group that owns a stage (it writes p, m, v)
 // Commit barriers per layer, one per tile in rotation; a waiter must never
 // see its barrier lapped.  While an epilogue thread waits for tile j, the
 // slots of j and of the later tiles of its stage stay taken, so the MMA
@@ -517,11 +519,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
     sessions([&](int32_t u0, int32_t u1, int32_t K) {
 
         // --------------------------- feature warpgroups ------------------------
-        // Group grp owns the stages n with n % 2 == grp and builds the A
-        // operand of layer 1 for each of their tiles in order.
+        // Group grp owns the stages n with n % 2 == grp: it builds the A
+        // operand of layer 1 for each of their tiles in order, then finishes
+        // each tile once its layer-2 result is in (ReLU(h2), output layer,
+        // update of p in the stage).
         const int grp = (warp - kFeatWarp0) >> 2;
         const int t = tid - 32 * kFeatWarp0 - 128 * grp;
         const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
+        const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
+        const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
+        const float lr = a.lr, wd = a.wd;
         StageIter si;
         si.init(a.units, a.desc, u0, u1);
         bool ok = true;
@@ -646,82 +654,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             tc_fence_before();
             mbar_arrive(a1_full + held);
           }
-          fence_proxy_async();   // m, v in the stage, before its write-back
-          mbar_arrive(stage_done + si.st);
-        }
-    });
-  } else {
-    sessions([&](int32_t u0, int32_t u1, int32_t K) {
-
-        // ------------------------------ epilogue -------------------------------
-        // Group h owns the stages n with n % 2 == h.  For a stage it first
-        // finishes layer 1 of every tile (ReLU, FP16 A operand of layer 2, b2
-        // preset of its accumulator), then the rest of every tile (ReLU(h2),
-        // output layer, update of p in the stage).
-        const int h = warp >> 2;
-        const int t = tid - 128 * h;
-        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
-        const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
-        const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
-        const float lr = a.lr, wd = a.wd;
-        StageIter si;
-        si.init(a.units, a.desc, u0, u1);
-        bool ok = true;
-        for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
-          if (ns % kEpiGroups != h) continue;
-          // the stage's record (written by the producer before it was loaded)
-          if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
+          {
+          // ---- the rest of every tile of the stage, two tiles at a time (a
+          // stage has a multiple of four), so that every output-layer weight
+          // read from shared memory serves two elements; a slot is freed as
+          // soon as its h2 is read.  Lane t of the stage's tiles holds this
+          // thread's own elements.
+          float* const pst = sbase;
           const int ntl = stage_tiles(si.n);
-          const int s0 = si.k0 % S;
-          // ---- layer 1 of every tile, two tiles at a time: the b2 preset is
-          // read from shared memory once for both
-          int s = s0;
-          for (int j = 0; j < ntl; j += 2) {
-            const int s1 = s + 1 == S ? 0 : s + 1;
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-              const int32_t k = si.k0 + j + tt;
-              if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t col = t_lane + (tt ? s1 : s) * G::SlotCols;
-              uint32_t av[16];
-              {
-                uint32_t h1[NP];
-                tmem_ld_row<NP>(col, h1);
-                tmem_wait_ld();
-                pack_relu_row<NP>(h1, av);
-              }
-              tmem_st16(col + NP, av);
-            }
-            if (!ok) break;
-            uint32_t b2[NP];
-#pragma unroll
-            for (int q = 0; q < NP; q += 4) {
-              const float4 b = *reinterpret_cast<const float4*>(aux + q);
-              b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
-              b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
-            }
-            tmem_st_row<NP>(t_lane + s * G::SlotCols, b2);
-            tmem_st_row<NP>(t_lane + s1 * G::SlotCols, b2);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(a2_full + s);
-            mbar_arrive(a2_full + s1);
-            s = s1 + 1 == S ? 0 : s1 + 1;
-          }
-          if (!ok) break;
-          // ---- the rest of every tile, two tiles at a time (a stage has a
-          // multiple of four), so that every output-layer weight read from
-          // shared memory serves two elements; a slot is freed as soon as its
-          // h2 is read
-          const StageRec& rc = rec[si.st];
-          const bool stg = rc.bytes != 0;
-          float* const pst = ring + si.st * (kArrays * kStageElems);
-          s = s0;
+          int s = si.k0 % S;
           for (int j = 0; j < ntl; j += 2) {
             const int32_t k = si.k0 + j;
             if (!mbar_wait_or_abort(done2 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag) ||
@@ -786,9 +727,70 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
               }
             }
           }
+          }
           if (!ok) break;
-          fence_proxy_async();   // p in the stage, before its write-back
+          fence_proxy_async();   // p, m, v in the stage, before its write-back
           mbar_arrive(stage_done + si.st);
+        }
+    });
+  } else {
+    sessions([&](int32_t u0, int32_t u1, int32_t K) {
+
+        // ------------------------------ epilogue -------------------------------
+        // Group h owns the stages n with n % 2 == h and finishes layer 1 of
+        // every tile of them (ReLU, FP16 A operand of layer 2, b2 preset of
+        // its accumulator).  The rest of a tile (ReLU(h2), output layer,
+        // update of p) is done by the feature group that built it.
+        const int h = warp >> 2;
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
+        StageIter si;
+        si.init(a.units, a.desc, u0, u1);
+        bool ok = true;
+        for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
+          if (ns % kEpiGroups != h) continue;
+          const int ntl = stage_tiles(si.n);
+          const int s0 = si.k0 % S;
+          // ---- layer 1 of every tile, two tiles at a time: the b2 preset is
+          // read from shared memory once for both
+          int s = s0;
+          for (int j = 0; j < ntl; j += 2) {
+            const int s1 = s + 1 == S ? 0 : s + 1;
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+              const int32_t k = si.k0 + j + tt;
+              if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t col = t_lane + (tt ? s1 : s) * G::SlotCols;
+              uint32_t av[16];
+              {
+                uint32_t h1[NP];
+                tmem_ld_row<NP>(col, h1);
+                tmem_wait_ld();
+                pack_relu_row<NP>(h1, av);
+              }
+              tmem_st16(col + NP, av);
+            }
+            if (!ok) break;
+            uint32_t b2[NP];
+#pragma unroll
+            for (int q = 0; q < NP; q += 4) {
+              const float4 b = *reinterpret_cast<const float4*>(aux + q);
+              b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
+              b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
+            }
+            tmem_st_row<NP>(t_lane + s * G::SlotCols, b2);
+            tmem_st_row<NP>(t_lane + s1 * G::SlotCols, b2);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(a2_full + s);
+            mbar_arrive(a2_full + s1);
+            s = s1 + 1 == S ? 0 : s1 + 1;
+          }
+          if (!ok) break;
         }
     });
   }
