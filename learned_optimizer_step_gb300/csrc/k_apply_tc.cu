@@ -246,12 +246,6 @@ __device__ __forceinline__ void stage_row_col(const StageRec& rc, int xi, int64_
 
 __device__ __forceinline__ float2 ld_f2(const float* p) { return *reinterpret_cast<const float2*>(p); }
 __device__ __forceinline__ void st_f2(float* p, const float2& v) { *reinterpret_cast<float2*>(p) = v; }
-// Component e of a float2 (e a constant after unrolling).
-__device__ __forceinline__ float f2get(const float2& v, int e) { return e == 0 ? v.x : v.y; }
-__device__ __forceinline__ void f2set(float2& v, int e, float x) {
-  if (e == 0) v.x = x;
-  else v.y = x;
-}
 
 // Per-row terms of one element's features: rr = r / rho and sr = sqrt(r)
 // (as r * rsqrt(r + eps)), shared by every element of a row.
@@ -309,6 +303,66 @@ __device__ __forceinline__ void features_f16(float p, float g, float (&m)[3], fl
   }
   av[14] = 0x00003C00u;   // 1.0h (against b1 in the B operand), 0
   av[15] = 0u;
+}
+
+// features_f16 for two neighbouring elements of one row at once, one in
+// each half of every float2 (x: the first, y: the second), with the paired
+// FP32 instructions.  Every result is the same single-element operation as
+// in features_f16, so both elements get exactly its values.  srn: the row's
+// sqrt(r_k) features already normalised (sr_k * sc[13 + k]).
+__device__ __forceinline__ void features_f16_pair(float2 P, float2 G, float2 (&M)[3], float2& V,
+                                                  const float (&rr)[3], const float (&srn)[3],
+                                                  const float2 (&C)[3], const float* sc, uint32_t (&avA)[16],
+                                                  uint32_t (&avB)[16]) {
+  const auto dup = [](float x) { return make_float2(x, x); };
+#pragma unroll
+  for (int k = 0; k < 3; ++k) M[k] = __ffma2_rn(dup(beta(k)), M[k], __fmul2_rn(dup(one_minus_beta(k)), G));
+  V = __ffma2_rn(dup(kBeta2), V, __fmul2_rn(dup(kOneMinusBeta2), __fmul2_rn(G, G)));
+  const float2 ve = __fadd2_rn(V, dup(kEps));
+  const float2 rsv = make_float2(frsqrt(ve.x), frsqrt(ve.y));
+  float2 rvh[3], sq[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const float2 h = __ffma2_rn(dup(rr[k]), C[k], dup(kEps));
+    rvh[k] = make_float2(frsqrt(h.x), frsqrt(h.y));
+    const float2 ce = __fadd2_rn(C[k], dup(kEps));
+    sq[k] = __fmul2_rn(C[k], make_float2(frsqrt(ce.x), frsqrt(ce.y)));
+  }
+  // features 0-27 in order, normalised, two at a time into FP16 pairs
+  const float4* sc4 = reinterpret_cast<const float4*>(sc);
+  auto put = [&](int d2, float2 f0, float2 f1, float s0, float s1) {   // features 2 d2, 2 d2 + 1
+    const float2 n0 = __fmul2_rn(f0, dup(s0)), n1 = __fmul2_rn(f1, dup(s1));
+    avA[d2] = f16x2(n0.x, n1.x);
+    avB[d2] = f16x2(n0.y, n1.y);
+  };
+  float4 s;
+  s = sc4[0];
+  put(0, P, G, s.x, s.y);
+  put(1, M[0], M[1], s.z, s.w);
+  s = sc4[1];
+  put(2, M[2], __fmul2_rn(V, rsv), s.x, s.y);
+  put(3, __fmul2_rn(M[0], rsv), __fmul2_rn(M[1], rsv), s.z, s.w);
+  s = sc4[2];
+  put(4, __fmul2_rn(M[2], rsv), __fmul2_rn(G, rsv), s.x, s.y);
+  put(5, __fmul2_rn(G, rvh[0]), __fmul2_rn(G, rvh[1]), s.z, s.w);
+  s = sc4[3];
+  {  // g rsqrt(vhat_2), then the first normalised sqrt(r) of the row
+    const float2 n0 = __fmul2_rn(__fmul2_rn(G, rvh[2]), dup(s.x));
+    avA[6] = f16x2(n0.x, srn[0]);
+    avB[6] = f16x2(n0.y, srn[0]);
+  }
+  avA[7] = avB[7] = f16x2(srn[1], srn[2]);
+  s = sc4[4];
+  put(8, sq[0], sq[1], s.x, s.y);
+  put(9, sq[2], __fmul2_rn(M[0], rvh[0]), s.z, s.w);
+  s = sc4[5];
+  put(10, __fmul2_rn(M[0], rvh[1]), __fmul2_rn(M[0], rvh[2]), s.x, s.y);
+  put(11, __fmul2_rn(M[1], rvh[0]), __fmul2_rn(M[1], rvh[1]), s.z, s.w);
+  s = sc4[6];
+  put(12, __fmul2_rn(M[1], rvh[2]), __fmul2_rn(M[2], rvh[0]), s.x, s.y);
+  put(13, __fmul2_rn(M[2], rvh[1]), __fmul2_rn(M[2], rvh[2]), s.z, s.w);
+  avA[14] = avB[14] = 0x00003C00u;   // 1.0h (against b1 in the B operand), 0
+  avA[15] = avB[15] = 0u;
 }
 
 template <int NP>
@@ -554,6 +608,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             if (++s == S) { s = 0; sph ^= 1u; }
             return true;
           };
+          // The same for two tiles at once (one wait for both stores).
+          auto emit_pair = [&](const uint32_t (&avA)[16], const uint32_t (&avB)[16]) -> bool {
+            const int s1 = s + 1 == S ? 0 : s + 1;
+            const uint32_t ph1 = s1 == 0 ? sph ^ 1u : sph;
+            if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag) ||
+                !mbar_wait_or_abort(slot_empty + s1, ph1 ^ 1u, kWaitNs, abort_flag))
+              return false;
+            tmem_st16(t_lane + s * G::SlotCols + NP, avA);
+            tmem_st16(t_lane + s1 * G::SlotCols + NP, avB);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(a1_full + s);
+            mbar_arrive(a1_full + s1);
+            s = s1 + 1 == S ? 0 : s1 + 1;
+            if (s1 == 0 || s == 0) sph ^= 1u;   // passed the end of the ring
+            return true;
+          };
           for (int qd = 0; ok && qd < nq; ++qd) {
             const int x0 = qd * kQuadElems + 4 * t;   // this lane's first element in the stage
             if (rc.quad) {
@@ -570,31 +641,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
                 inv_rho[q] = rc.inv_rho[q];
               }
               row_terms_f16(r, inv_rho, rr, sr);
-              // two pairs of elements, 64-bit loads and stores
+              float srn[3];
+#pragma unroll
+              for (int q = 0; q < 3; ++q) srn[q] = fmul(sr[q], rc.sc[13 + q]);
+              // two pairs of elements, 64-bit loads and stores; each pair is
+              // built at once and handed to tiles 4 qd + h and 4 qd + h + 1
 #pragma unroll
               for (int h = 0; h < 4; h += 2) {
                 const int xh = x0 + h;
                 const float2 P = ld_f2(sbase + xh), Gr = ld_f2(sbase + kStageElems + xh);
-                float2 M0 = ld_f2(sbase + 2 * kStageElems + xh), M1 = ld_f2(sbase + 3 * kStageElems + xh);
-                float2 M2 = ld_f2(sbase + 4 * kStageElems + xh), V = ld_f2(sbase + 5 * kStageElems + xh);
+                float2 M[3] = {ld_f2(sbase + 2 * kStageElems + xh), ld_f2(sbase + 3 * kStageElems + xh),
+                               ld_f2(sbase + 4 * kStageElems + xh)};
+                float2 V = ld_f2(sbase + 5 * kStageElems + xh);
                 float2 c2[3];
 #pragma unroll
                 for (int q = 0; q < 3; ++q) c2[q] = __ldg(reinterpret_cast<const float2*>(rc.c[q] + jc + h));
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  float m[3] = {f2get(M0, e), f2get(M1, e), f2get(M2, e)};
-                  float v = f2get(V, e);
-                  const float c[3] = {f2get(c2[0], e), f2get(c2[1], e), f2get(c2[2], e)};
-                  // normalised features, FP16, for this lane's row of the A
-                  // operand of tile 4 qd + h + e (K = 32: 28 features, 1, 0s)
-                  uint32_t av[16];
-                  features_f16(f2get(P, e), f2get(Gr, e), m, v, rr, sr, c, rc.sc, av);
-                  f2set(M0, e, m[0]); f2set(M1, e, m[1]); f2set(M2, e, m[2]); f2set(V, e, v);
-                  if (!emit(av)) { ok = false; break; }
-                }
-                if (!ok) break;
-                st_f2(sbase + 2 * kStageElems + xh, M0); st_f2(sbase + 3 * kStageElems + xh, M1);
-                st_f2(sbase + 4 * kStageElems + xh, M2); st_f2(sbase + 5 * kStageElems + xh, V);
+                // normalised features, FP16, for this lane's row of the A
+                // operands (K = 32: 28 features, 1, 0s)
+                uint32_t avA[16], avB[16];
+                features_f16_pair(P, Gr, M, V, rr, srn, c2, rc.sc, avA, avB);
+                st_f2(sbase + 2 * kStageElems + xh, M[0]); st_f2(sbase + 3 * kStageElems + xh, M[1]);
+                st_f2(sbase + 4 * kStageElems + xh, M[2]); st_f2(sbase + 5 * kStageElems + xh, V);
+                if (!emit_pair(avA, avB)) { ok = false; break; }
               }
               if (!ok) break;
             } else {
