@@ -12,18 +12,18 @@
 //   warp 16      producer: bulk-copies (cp.async.bulk, one array per lane) p,
 //                g, m0..2, v of up to 8 tiles (a stage) of a work unit into a
 //                ring of shared-memory stages, and writes p, m0..2, v of a
-//                stage back with bulk copies once its feature group is done;
+//                stage back with bulk copies once its two groups are done;
 //   warps 8-15   two feature warpgroups, owning alternate stages: EMA
 //                update, features, normalisation, FP16 A operand of layer 1
 //                into the tile slot's tensor memory (the updated m and v go
-//                back into the stage); then, for the same tiles, once their
-//                layer-2 result is in: ReLU(h2), the two-unit output layer
-//                in FP32 on the CUDA cores, and the update of p in the stage
-//                (lane t of a stage's tiles holds the thread's own elements);
-//   warps 17-18  MMA issuers, one thread each: layer 1 and layer 2;
+//                back into the stage), two elements (two tiles) at a time;
+//   warps 17-18  MMA issuers, one thread each: layer 1 and layer 2, two
+//                tiles and one commit at a time;
 //   warps 0-7    two epilogue warpgroups, owning alternate stages, two
 //                tiles at a time: ReLU + FP16 A operand of layer 2 (in
-//                tensor memory) and the b2 preset of its accumulator.
+//                tensor memory) and the b2 preset of its accumulator; and,
+//                two pairs later, ReLU(h2), the two-unit output layer in
+//                FP32 on the CUDA cores and the update of p in the stage.
 // A tile is 128 elements of one tensor (one per TMEM lane); four tiles
 // cover 512 consecutive elements, lane t of each holding one of elements
 // 4t..4t+3, so that a feature thread finds the row of four consecutive
@@ -35,21 +35,22 @@
 // small record, so the feature warps keep no per-tensor state.  Owning whole
 // stages keeps the per-tile control flow of the warps small.
 //
-// A small MMA (M=128, N<=32) keeps its issuing thread about 120 cycles,
-// whatever its N (measured: 122-162 cycles for N from 16 to 256), and about
-// 130 cycles more pass from its commit to a waiting thread.  So a tile uses few MMAs (FP16 operands, K = 32 for layer 1 with b1
-// against a constant 1 in the A operand, K = NP for layer 2 onto the preset
-// b2: 4 MMAs at NP = 32, one tcgen05.commit per layer and tile) and only two
-// MMA round trips: the output layer (two units) runs on the CUDA cores.  The
-// two layers are issued by two threads in different warps, which issue side
-// by side.  At
-// most S tiles are in flight (10 slots at NP = 32), and a tile keeps its
-// slot from its features to the read of its layer-2 result, so S tiles per
-// slot lifetime bound the throughput.  Much of that lifetime is the wait for
-// an epilogue group; hence the epilogue's two tiles at a time (shared reads
-// of b2), the second half of each tile's epilogue in the feature groups
-// (which have slack), and no third MMA for the output layer: its round trip
-// lengthens the lifetime more than it shortens the epilogue.
+// Issuing is the scarce resource of the tensor-core side: measured on one
+// SM, a thread that issues two small MMAs (M=128, N=32, K=16) per tile
+// spends about 150 cycles on them and about 185 more on a commit, while
+// threads of different warps issue side by side.  So a tile uses few MMAs
+// (FP16 operands, K = 32 for layer 1 with b1 against a constant 1 in the A
+// operand, K = NP for layer 2 onto the preset b2: 4 MMAs at NP = 32), a
+// commit covers two tiles, and only two MMA round trips are made: the
+// output layer (two units) runs on the CUDA cores.  (More issuer warps were
+// measured to slow the kernel: their polling takes issue slots from the
+// feature warps.)  At most S tiles are in flight (10 slots at NP = 32), and
+// a tile keeps its slot from its features to the read of its layer-2
+// result, so S tiles per slot lifetime bound the throughput; hence the
+// epilogue's lag of two pairs between layer 1 and the rest of a pair (by
+// then layer 2 has usually completed), and no third MMA for the output
+// layer: its round trip lengthens the lifetime more than it shortens the
+// epilogue.
 //
 // The tiles of a CTA are processed in sessions: maximal runs of tiles whose
 // tensors share one MLP weight set.  Between sessions the pipeline drains,
@@ -83,12 +84,15 @@ constexpr int kStageElems = kStageTiles * kTile;
 constexpr int kArrays = 6;                // p, g, m0, m1, m2, v
 constexpr int kRingStages = 6;            // stages held in shared memory
 constexpr int kStageBytes = kArrays * kStageElems * 4;
-constexpr int kStageUsers = kTile;        // the feature group that owns a stage (it writes p, m, v)
-// Commit barriers per layer, one per tile in rotation; a waiter must never
-// see its barrier lapped.  While an epilogue thread waits for tile j, the
-// slots of j and of the later tiles of its stage stay taken, so the MMA
-// threads can get no further ahead than the stages the other epilogue groups
-// own plus one slot round: fewer than kEpiGroups * kStageTiles + S tiles.
+constexpr int kStageUsers = 2 * kTile;    // the feature group (m, v) and the epilogue group (p) of a stage
+// An epilogue group finishes a pair of tiles this many pairs after its layer 1.
+constexpr int kLag = 2;
+// Commit barriers per layer, one per pair of tiles in rotation; a waiter
+// must never see its barrier lapped.  While an epilogue thread waits for
+// pair j, the slots of j and of the later tiles of its stage stay taken, so
+// the MMA threads can get no further ahead than the stages the other
+// epilogue groups own plus one slot round: fewer than kEpiGroups *
+// kStageTiles + S tiles, well under kDone pairs.
 constexpr int kDone = 64;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -148,6 +152,7 @@ struct Geom {
   static_assert(Smem <= 232448, "shared memory of one CTA");
   // a feature group emits all tiles of a stage before it finishes any: the
   // stage's last tile must not wait for a slot of its own
+  static_assert(S % 2 == 0, "tile pairs start on even slots");
   static_assert(S * SlotCols <= 512 && S > kStageTiles && kDone >= kEpiGroups * kStageTiles + S,
                 "tensor memory columns / pipeline depth");
   static_assert(oRec % 16 == 0 && sizeof(StageRec) % 16 == 0, "16-byte aligned stage records");
@@ -540,9 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       } else if (warp == kMma1Warp || warp == kMma2Warp) {
 
           // ------------------------------ MMA issuers ----------------------------
-          // One thread per layer: layer 1 of tile k once its A operand is in
-          // tensor memory, committed to done1[k]; layer 2 of tile k once its A
-          // operand and b2 preset are, committed to done2[k].
+          // One thread per layer, two tiles at a time (tiles come in pairs):
+          // layer 1 of tiles k, k + 1 once their A operands are in tensor
+          // memory, committed to done1[k / 2]; layer 2 once their A operands
+          // and b2 presets are, committed to done2[k / 2].  A commit keeps the
+          // issuing thread about as long as two MMAs, so one per pair.
           if (lane == 0) {
             const bool l1 = warp == kMma1Warp;
             const uint64_t dB = l1 ? smem_desc(s_base + G::oB1, 128, G::SBO1) : smem_desc(s_base + G::oB2, 128, G::SBO);
@@ -551,19 +558,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             const int ksteps = l1 ? 2 : NP / 16;   // K-steps of 16 FP16 values (8 A columns)
             int s = 0;
             uint32_t ph = 0;
-            int k = 0;
-            for (; k < K; ++k) {
-              if (!mbar_wait_or_abort(full + s, ph, kWaitNs, abort_flag)) break;
+            int32_t k = 0;
+            for (; k < K; k += 2) {
+              const int s1 = s + 1;   // S is even and pairs start on even tiles
+              if (!mbar_wait_or_abort(full + s, ph, kWaitNs, abort_flag) ||
+                  !mbar_wait_or_abort(full + s1, ph, kWaitNs, abort_flag))
+                break;
               tc_fence_after();
-              const uint32_t d = tmem + s * G::SlotCols;
-              // layer 1 overwrites its accumulator; layer 2 adds onto the b2 preset
-              mma_f16_ts(d, d + NP, dB, G::ID12, l1 ? 0u : 1u);
-              if (ksteps > 1) mma_f16_ts(d, d + NP + 8, dB + 16, G::ID12, 1u);
-              mma_commit(fin + (k & (kDone - 1)));   // tracks every MMA of this thread so far
-              if (++s == S) { s = 0; ph ^= 1u; }
+#pragma unroll
+              for (int tt = 0; tt < 2; ++tt) {
+                const uint32_t d = tmem + (tt ? s1 : s) * G::SlotCols;
+                // layer 1 overwrites its accumulator; layer 2 adds onto the b2 preset
+                mma_f16_ts(d, d + NP, dB, G::ID12, l1 ? 0u : 1u);
+                if (ksteps > 1) mma_f16_ts(d, d + NP + 8, dB + 16, G::ID12, 1u);
+              }
+              mma_commit(fin + ((k >> 1) & (kDone - 1)));   // tracks every MMA of this thread so far
+              s += 2;
+              if (s == S) { s = 0; ph ^= 1u; }
             }
             // nothing of ours may still be running when the session ends
-            if (k > 0) mbar_drain(fin + ((k - 1) & (kDone - 1)), (uint32_t)(((k - 1) / kDone) & 1), kWaitNs / 10);
+            if (k > 0) {
+              const int32_t kp = (k - 2) >> 1;
+              mbar_drain(fin + (kp & (kDone - 1)), (uint32_t)((kp / kDone) & 1), kWaitNs / 10);
+            }
           }
       }
     });
@@ -571,17 +588,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
     sessions([&](int32_t u0, int32_t u1, int32_t K) {
 
         // --------------------------- feature warpgroups ------------------------
-        // Group grp owns the stages n with n % 2 == grp: it builds the A
-        // operand of layer 1 for each of their tiles in order, then finishes
-        // each tile once its layer-2 result is in (ReLU(h2), output layer,
-        // update of p in the stage).
+        // Group grp owns the stages n with n % 2 == grp: it updates m and v
+        // in the stage and builds the A operand of layer 1 for each of their
+        // tiles in order.
         const int grp = (warp - kFeatWarp0) >> 2;
         const int t = tid - 32 * kFeatWarp0 - 128 * grp;
         const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
-        const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
-        const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
-        const float lr = a.lr, wd = a.wd;
         StageIter si;
         si.init(a.units, a.desc, u0, u1);
         bool ok = true;
@@ -710,24 +722,88 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             }
           }
           if (!ok) break;
-          {
-          // ---- the rest of every tile of the stage, two tiles at a time (a
-          // stage has a multiple of four), so that every output-layer weight
-          // read from shared memory serves two elements; a slot is freed as
-          // soon as its h2 is read.  Lane t of the stage's tiles holds this
-          // thread's own elements.
-          float* const pst = sbase;
+          fence_proxy_async();   // m, v in the stage, before its write-back
+          mbar_arrive(stage_done + si.st);
+        }
+    });
+  } else {
+    sessions([&](int32_t u0, int32_t u1, int32_t K) {
+
+        // ------------------------------ epilogue -------------------------------
+        // Group h owns the stages n with n % 2 == h.  For each pair of tiles
+        // of a stage it finishes layer 1 (ReLU, FP16 A operand of layer 2, b2
+        // preset of its accumulator) and, kLag pairs later, the rest (ReLU(h2),
+        // output layer, update of p in the stage): by then the pair's layer 2
+        // has usually completed, so neither step waits for the tensor cores.
+        const int h = warp >> 2;
+        const int t = tid - 128 * h;
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
+        const float4* w3 = reinterpret_cast<const float4*>(aux + NP);   // {w0_j, w0_j+1, w1_j, w1_j+1}
+        const float b30 = aux[3 * NP], b31 = aux[3 * NP + 1];
+        const float lr = a.lr, wd = a.wd;
+        StageIter si;
+        si.init(a.units, a.desc, u0, u1);
+        bool ok = true;
+        for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
+          if (ns % kEpiGroups != h) continue;
+          // the stage's record and p (loaded before any of its tiles was built)
+          if (!mbar_wait_or_abort(ring_full + si.st, si.ph, kWaitNs, abort_flag)) { ok = false; break; }
+          const StageRec& rc = rec[si.st];
+          const bool stg = rc.bytes != 0;
+          float* const pst = ring + si.st * (kArrays * kStageElems);
           const int ntl = stage_tiles(si.n);
-          int s = si.k0 % S;
-          for (int j = 0; j < ntl; j += 2) {
-            const int32_t k = si.k0 + j;
-            if (!mbar_wait_or_abort(done2 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag) ||
-                !mbar_wait_or_abort(done2 + ((k + 1) & (kDone - 1)), (uint32_t)(((k + 1) / kDone) & 1), kWaitNs,
-                                    abort_flag)) {
-              ok = false;
-              break;
+          const int s0 = si.k0 % S;
+
+          // ---- layer 1 of tiles j, j + 1: the b2 preset is read from shared
+          // memory once for both
+          auto layer1 = [&](int j) -> bool {
+            const int s = (s0 + j) % S;
+            const int s1 = s + 1 == S ? 0 : s + 1;
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+              const int32_t k = si.k0 + j + tt;
+              if (tt == 0 && !mbar_wait_or_abort(done1 + ((k >> 1) & (kDone - 1)), (uint32_t)(((k >> 1) / kDone) & 1),
+                                                 kWaitNs, abort_flag))
+                return false;
+              tc_fence_after();
+              const uint32_t col = t_lane + (tt ? s1 : s) * G::SlotCols;
+              uint32_t av[16];
+              {
+                uint32_t h1[NP];
+                tmem_ld_row<NP>(col, h1);
+                tmem_wait_ld();
+                pack_relu_row<NP>(h1, av);
+              }
+              tmem_st16(col + NP, av);
             }
+            uint32_t b2[NP];
+#pragma unroll
+            for (int q = 0; q < NP; q += 4) {
+              const float4 b = *reinterpret_cast<const float4*>(aux + q);
+              b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
+              b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
+            }
+            tmem_st_row<NP>(t_lane + s * G::SlotCols, b2);
+            tmem_st_row<NP>(t_lane + s1 * G::SlotCols, b2);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(a2_full + s);
+            mbar_arrive(a2_full + s1);
+            return true;
+          };
+
+          // ---- the rest of tiles j, j + 1, so that every output-layer weight
+          // read from shared memory serves two elements; their slots are freed
+          // as soon as h2 is read.  Lane t of the stage's tiles holds this
+          // thread's elements.
+          auto finish = [&](int j) -> bool {
+            const int32_t k = si.k0 + j;
+            if (!mbar_wait_or_abort(done2 + ((k >> 1) & (kDone - 1)), (uint32_t)(((k >> 1) / kDone) & 1), kWaitNs,
+                                    abort_flag))
+              return false;
             tc_fence_after();
+            const int s = (s0 + j) % S;
             const int s1 = s + 1 == S ? 0 : s + 1;
             // output layer: (direction, magnitude) = ReLU(h2) . W3 + b3 for
             // both tiles, over 16 hidden units at a time, two FMA chains each
@@ -763,7 +839,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
                 }
               }
             }
-            s = s1 + 1 == S ? 0 : s1 + 1;
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt) {
               const float o0 = (acc[tt][0].x + acc[tt][0].y) + (acc[tt][2].x + acc[tt][2].y) + b30;
@@ -782,71 +857,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
                 *pp = *pp - lr * (upd + wd * *pp);
               }
             }
-          }
-          }
-          if (!ok) break;
-          fence_proxy_async();   // p, m, v in the stage, before its write-back
-          mbar_arrive(stage_done + si.st);
-        }
-    });
-  } else {
-    sessions([&](int32_t u0, int32_t u1, int32_t K) {
+            return true;
+          };
 
-        // ------------------------------ epilogue -------------------------------
-        // Group h owns the stages n with n % 2 == h and finishes layer 1 of
-        // every tile of them (ReLU, FP16 A operand of layer 2, b2 preset of
-        // its accumulator).  The rest of a tile (ReLU(h2), output layer,
-        // update of p) is done by the feature group that built it.
-        const int h = warp >> 2;
-        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-        const float* aux = reinterpret_cast<const float*>(smem + G::oB2 + G::B2);
-        StageIter si;
-        si.init(a.units, a.desc, u0, u1);
-        bool ok = true;
-        for (int32_t ns = 0; ok && si.valid(); ++ns, si.next()) {
-          if (ns % kEpiGroups != h) continue;
-          const int ntl = stage_tiles(si.n);
-          const int s0 = si.k0 % S;
-          // ---- layer 1 of every tile, two tiles at a time: the b2 preset is
-          // read from shared memory once for both
-          int s = s0;
-          for (int j = 0; j < ntl; j += 2) {
-            const int s1 = s + 1 == S ? 0 : s + 1;
-#pragma unroll
-            for (int tt = 0; tt < 2; ++tt) {
-              const int32_t k = si.k0 + j + tt;
-              if (!mbar_wait_or_abort(done1 + (k & (kDone - 1)), (uint32_t)((k / kDone) & 1), kWaitNs, abort_flag)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              const uint32_t col = t_lane + (tt ? s1 : s) * G::SlotCols;
-              uint32_t av[16];
-              {
-                uint32_t h1[NP];
-                tmem_ld_row<NP>(col, h1);
-                tmem_wait_ld();
-                pack_relu_row<NP>(h1, av);
-              }
-              tmem_st16(col + NP, av);
-            }
-            if (!ok) break;
-            uint32_t b2[NP];
-#pragma unroll
-            for (int q = 0; q < NP; q += 4) {
-              const float4 b = *reinterpret_cast<const float4*>(aux + q);
-              b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
-              b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
-            }
-            tmem_st_row<NP>(t_lane + s * G::SlotCols, b2);
-            tmem_st_row<NP>(t_lane + s1 * G::SlotCols, b2);
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(a2_full + s);
-            mbar_arrive(a2_full + s1);
-            s = s1 + 1 == S ? 0 : s1 + 1;
+          for (int j = 0; ok && j < ntl; j += 2) {
+            ok = layer1(j);
+            if (ok && j >= 2 * kLag) ok = finish(j - 2 * kLag);
           }
+          for (int j = ntl > 2 * kLag ? ntl - 2 * kLag : 0; ok && j < ntl; j += 2) ok = finish(j);
           if (!ok) break;
+          fence_proxy_async();   // p in the stage, before its write-back
+          mbar_arrive(stage_done + si.st);
         }
     });
   }
