@@ -314,60 +314,74 @@ __device__ __forceinline__ void features_f16(float p, float g, float (&m)[3], fl
 // each half of every float2 (x: the first, y: the second), with the paired
 // FP32 instructions.  Every result is the same single-element operation as
 // in features_f16, so both elements get exactly its values.  srn: the row's
-// sqrt(r_k) features already normalised (sr_k * sc[13 + k]).
-__device__ __forceinline__ void features_f16_pair(float2 P, float2 G, float2 (&M)[3], float2& V,
+// sqrt(r_k) features already normalised (sr_k * sc[13 + k]).  The FP16 words
+// come in two halves, to keep fewer registers live: words 0-7 (features
+// 0-15) of both elements go to store_lo(loA, loB), which returns false to
+// stop; words 8-15 (features 16-27, the constant 1, zeros) are returned.
+template <typename StoreLo>
+__device__ __forceinline__ bool features_f16_pair(float2 P, float2 G, float2 (&M)[3], float2& V,
                                                   const float (&rr)[3], const float (&srn)[3],
-                                                  const float2 (&C)[3], const float* sc, uint32_t (&avA)[16],
-                                                  uint32_t (&avB)[16]) {
+                                                  const float2 (&C)[3], const float* sc, StoreLo&& store_lo,
+                                                  uint32_t (&hiA)[8], uint32_t (&hiB)[8]) {
   const auto dup = [](float x) { return make_float2(x, x); };
 #pragma unroll
   for (int k = 0; k < 3; ++k) M[k] = __ffma2_rn(dup(beta(k)), M[k], __fmul2_rn(dup(one_minus_beta(k)), G));
   V = __ffma2_rn(dup(kBeta2), V, __fmul2_rn(dup(kOneMinusBeta2), __fmul2_rn(G, G)));
   const float2 ve = __fadd2_rn(V, dup(kEps));
   const float2 rsv = make_float2(frsqrt(ve.x), frsqrt(ve.y));
-  float2 rvh[3], sq[3];
+  float2 rvh[3];
 #pragma unroll
   for (int k = 0; k < 3; ++k) {
     const float2 h = __ffma2_rn(dup(rr[k]), C[k], dup(kEps));
     rvh[k] = make_float2(frsqrt(h.x), frsqrt(h.y));
-    const float2 ce = __fadd2_rn(C[k], dup(kEps));
-    sq[k] = __fmul2_rn(C[k], make_float2(frsqrt(ce.x), frsqrt(ce.y)));
   }
   // features 0-27 in order, normalised, two at a time into FP16 pairs
   const float4* sc4 = reinterpret_cast<const float4*>(sc);
-  auto put = [&](int d2, float2 f0, float2 f1, float s0, float s1) {   // features 2 d2, 2 d2 + 1
+  auto put = [&](uint32_t (&oa)[8], uint32_t (&ob)[8], int w, float2 f0, float2 f1, float s0, float s1) {
     const float2 n0 = __fmul2_rn(f0, dup(s0)), n1 = __fmul2_rn(f1, dup(s1));
-    avA[d2] = f16x2(n0.x, n1.x);
-    avB[d2] = f16x2(n0.y, n1.y);
+    oa[w] = f16x2(n0.x, n1.x);
+    ob[w] = f16x2(n0.y, n1.y);
   };
-  float4 s;
-  s = sc4[0];
-  put(0, P, G, s.x, s.y);
-  put(1, M[0], M[1], s.z, s.w);
-  s = sc4[1];
-  put(2, M[2], __fmul2_rn(V, rsv), s.x, s.y);
-  put(3, __fmul2_rn(M[0], rsv), __fmul2_rn(M[1], rsv), s.z, s.w);
-  s = sc4[2];
-  put(4, __fmul2_rn(M[2], rsv), __fmul2_rn(G, rsv), s.x, s.y);
-  put(5, __fmul2_rn(G, rvh[0]), __fmul2_rn(G, rvh[1]), s.z, s.w);
-  s = sc4[3];
-  {  // g rsqrt(vhat_2), then the first normalised sqrt(r) of the row
-    const float2 n0 = __fmul2_rn(__fmul2_rn(G, rvh[2]), dup(s.x));
-    avA[6] = f16x2(n0.x, srn[0]);
-    avB[6] = f16x2(n0.y, srn[0]);
+  {
+    uint32_t loA[8], loB[8];
+    float4 s;
+    s = sc4[0];
+    put(loA, loB, 0, P, G, s.x, s.y);
+    put(loA, loB, 1, M[0], M[1], s.z, s.w);
+    s = sc4[1];
+    put(loA, loB, 2, M[2], __fmul2_rn(V, rsv), s.x, s.y);
+    put(loA, loB, 3, __fmul2_rn(M[0], rsv), __fmul2_rn(M[1], rsv), s.z, s.w);
+    s = sc4[2];
+    put(loA, loB, 4, __fmul2_rn(M[2], rsv), __fmul2_rn(G, rsv), s.x, s.y);
+    put(loA, loB, 5, __fmul2_rn(G, rvh[0]), __fmul2_rn(G, rvh[1]), s.z, s.w);
+    s = sc4[3];
+    {  // g rsqrt(vhat_2), then the first normalised sqrt(r) of the row
+      const float2 n0 = __fmul2_rn(__fmul2_rn(G, rvh[2]), dup(s.x));
+      loA[6] = f16x2(n0.x, srn[0]);
+      loB[6] = f16x2(n0.y, srn[0]);
+    }
+    loA[7] = loB[7] = f16x2(srn[1], srn[2]);
+    if (!store_lo(loA, loB)) return false;
   }
-  avA[7] = avB[7] = f16x2(srn[1], srn[2]);
+  float2 sq[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    const float2 ce = __fadd2_rn(C[k], dup(kEps));
+    sq[k] = __fmul2_rn(C[k], make_float2(frsqrt(ce.x), frsqrt(ce.y)));
+  }
+  float4 s;
   s = sc4[4];
-  put(8, sq[0], sq[1], s.x, s.y);
-  put(9, sq[2], __fmul2_rn(M[0], rvh[0]), s.z, s.w);
+  put(hiA, hiB, 0, sq[0], sq[1], s.x, s.y);
+  put(hiA, hiB, 1, sq[2], __fmul2_rn(M[0], rvh[0]), s.z, s.w);
   s = sc4[5];
-  put(10, __fmul2_rn(M[0], rvh[1]), __fmul2_rn(M[0], rvh[2]), s.x, s.y);
-  put(11, __fmul2_rn(M[1], rvh[0]), __fmul2_rn(M[1], rvh[1]), s.z, s.w);
+  put(hiA, hiB, 2, __fmul2_rn(M[0], rvh[1]), __fmul2_rn(M[0], rvh[2]), s.x, s.y);
+  put(hiA, hiB, 3, __fmul2_rn(M[1], rvh[0]), __fmul2_rn(M[1], rvh[1]), s.z, s.w);
   s = sc4[6];
-  put(12, __fmul2_rn(M[1], rvh[2]), __fmul2_rn(M[2], rvh[0]), s.x, s.y);
-  put(13, __fmul2_rn(M[2], rvh[1]), __fmul2_rn(M[2], rvh[2]), s.z, s.w);
-  avA[14] = avB[14] = 0x00003C00u;   // 1.0h (against b1 in the B operand), 0
-  avA[15] = avB[15] = 0u;
+  put(hiA, hiB, 4, __fmul2_rn(M[1], rvh[2]), __fmul2_rn(M[2], rvh[0]), s.x, s.y);
+  put(hiA, hiB, 5, __fmul2_rn(M[2], rvh[1]), __fmul2_rn(M[2], rvh[2]), s.z, s.w);
+  hiA[6] = hiB[6] = 0x00003C00u;   // 1.0h (against b1 in the B operand), 0
+  hiA[7] = hiB[7] = 0u;
+  return true;
 }
 
 template <int NP>
@@ -620,22 +634,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             if (++s == S) { s = 0; sph ^= 1u; }
             return true;
           };
-          // The same for two tiles at once (one wait for both stores).
-          auto emit_pair = [&](const uint32_t (&avA)[16], const uint32_t (&avB)[16]) -> bool {
+          // The same for two tiles at once (one wait for both stores), in two
+          // steps: the slots are waited for and the first half of each A
+          // operand stored once it is built, then the second half stored and
+          // both tiles announced.
+          auto store_lo_pair = [&](const uint32_t (&loA)[8], const uint32_t (&loB)[8]) -> bool {
             const int s1 = s + 1 == S ? 0 : s + 1;
             const uint32_t ph1 = s1 == 0 ? sph ^ 1u : sph;
             if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag) ||
                 !mbar_wait_or_abort(slot_empty + s1, ph1 ^ 1u, kWaitNs, abort_flag))
               return false;
-            tmem_st16(t_lane + s * G::SlotCols + NP, avA);
-            tmem_st16(t_lane + s1 * G::SlotCols + NP, avB);
+            tmem_st8(t_lane + s * G::SlotCols + NP, loA);
+            tmem_st8(t_lane + s1 * G::SlotCols + NP, loB);
+            return true;
+          };
+          auto finish_emit_pair = [&](const uint32_t (&hiA)[8], const uint32_t (&hiB)[8]) {
+            const int s1 = s + 1 == S ? 0 : s + 1;
+            tmem_st8(t_lane + s * G::SlotCols + NP + 8, hiA);
+            tmem_st8(t_lane + s1 * G::SlotCols + NP + 8, hiB);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(a1_full + s);
             mbar_arrive(a1_full + s1);
             s = s1 + 1 == S ? 0 : s1 + 1;
             if (s1 == 0 || s == 0) sph ^= 1u;   // passed the end of the ring
-            return true;
           };
           for (int qd = 0; ok && qd < nq; ++qd) {
             const int x0 = qd * kQuadElems + 4 * t;   // this lane's first element in the stage
@@ -670,11 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
                 for (int q = 0; q < 3; ++q) c2[q] = __ldg(reinterpret_cast<const float2*>(rc.c[q] + jc + h));
                 // normalised features, FP16, for this lane's row of the A
                 // operands (K = 32: 28 features, 1, 0s)
-                uint32_t avA[16], avB[16];
-                features_f16_pair(P, Gr, M, V, rr, srn, c2, rc.sc, avA, avB);
+                uint32_t hiA[8], hiB[8];
+                if (!features_f16_pair(P, Gr, M, V, rr, srn, c2, rc.sc, store_lo_pair, hiA, hiB)) {
+                  ok = false;
+                  break;
+                }
                 st_f2(sbase + 2 * kStageElems + xh, M[0]); st_f2(sbase + 3 * kStageElems + xh, M[1]);
                 st_f2(sbase + 4 * kStageElems + xh, M[2]); st_f2(sbase + 5 * kStageElems + xh, V);
-                if (!emit_pair(avA, avB)) { ok = false; break; }
+                finish_emit_pair(hiA, hiB);
               }
               if (!ok) break;
             } else {
@@ -777,15 +802,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
               }
               tmem_st16(col + NP, av);
             }
-            uint32_t b2[NP];
 #pragma unroll
-            for (int q = 0; q < NP; q += 4) {
-              const float4 b = *reinterpret_cast<const float4*>(aux + q);
-              b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
-              b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
+            for (int hf = 0; hf < NP / 16; ++hf) {   // 16 columns at a time (fewer live registers)
+              uint32_t b2[16];
+#pragma unroll
+              for (int q = 0; q < 16; q += 4) {
+                const float4 b = *reinterpret_cast<const float4*>(aux + 16 * hf + q);
+                b2[q] = __float_as_uint(b.x); b2[q + 1] = __float_as_uint(b.y);
+                b2[q + 2] = __float_as_uint(b.z); b2[q + 3] = __float_as_uint(b.w);
+              }
+              tmem_st16(t_lane + s * G::SlotCols + 16 * hf, b2);
+              tmem_st16(t_lane + s1 * G::SlotCols + 16 * hf, b2);
             }
-            tmem_st_row<NP>(t_lane + s * G::SlotCols, b2);
-            tmem_st_row<NP>(t_lane + s1 * G::SlotCols, b2);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(a2_full + s);
