@@ -148,6 +148,27 @@ int lopt_set_mlp_path(lopt_handle h, int path);
 int lopt_set_weight_decay(lopt_handle h, float weight_decay);
 
 /*
+ * Single sweep through L2 for later lopt_step() calls.  With group_bytes >
+ * 0 the list is cut into groups of consecutive tensors whose state (p, g,
+ * m0..2, v: 24 bytes per element) is at most group_bytes, a larger tensor
+ * forming a group of its own, and each group runs the three kernels before
+ * the next group starts.  The statistics pass then reads g just after the
+ * row/column pass read it, and the apply pass reads p, g, m, v just after
+ * the statistics pass read them, so that with groups well inside the L2
+ * (129 MB on GB300) most of those re-reads come from L2 instead of DRAM.
+ * This is the pages' direction of keeping a tensor's state on chip between
+ * the two passes ("PyLO: Towards Accessible Learned Optimizers in PyTorch",
+ * sections "メモリ階層の活用" and "制約と今後の展望"), done by launch
+ * order.  Every statistic still covers a whole tensor, so results are the
+ * same bits as without groups.  Each group adds three launches and their
+ * start and end.  0 (the default) turns it off: one launch of each kernel
+ * over the whole list.  Row-sharded steps and host-buffer steps always use
+ * one group.  Kernel timing (lopt_kernel_times) sums each kernel over the
+ * groups.  Errors: LOPT_E_ARG (NULL handle or a negative size).
+ */
+int lopt_set_sweep_bytes(lopt_handle h, int64_t group_bytes);
+
+/*
  * One learned-optimizer step over n_tensors tensors (HOST array of
  * descriptors; it is read during the call only).
  *   t       1-based step count (drives the 11 time features tanh(t / x_s)).
@@ -155,7 +176,8 @@ int lopt_set_weight_decay(lopt_handle h, float weight_decay);
  *           by lopt_set_weight_decay()).
  *   stream  cudaStream_t to enqueue on (NULL = legacy default stream).
  * The whole list is processed by three kernel launches (row/column moments,
- * feature statistics, normalise + MLP + apply).  Asynchronous: returns once
+ * feature statistics, normalise + MLP + apply), or three per group of
+ * tensors after lopt_set_sweep_bytes().  Asynchronous: returns once
  * the work is enqueued.  Validation happens before anything is enqueued and
  * a failed validation leaves every buffer untouched.  Calls on one handle
  * are ordered with each other even across streams; a handle must not be

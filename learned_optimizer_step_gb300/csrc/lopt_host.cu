@@ -79,6 +79,14 @@ struct lopt_ctx {
   int w1fold_stride = 0;
   int n_units[3] = {0, 0, 0};
   int n_tensors = 0;
+  // L2-sized groups (lopt_set_sweep_bytes): per group, the first unit and
+  // the unit count of each kernel; empty: the whole list in one launch each
+  int64_t sweep_bytes = 0;
+  int64_t last_sweep = -1;
+  struct Group {
+    int first[3], count[3];
+  };
+  std::vector<Group> groups;
   // cached schedule key
   std::vector<lopt_tensor> last_list;
   std::vector<int64_t> last_grows;   // global rows of a row-sharded schedule (empty: plain)
@@ -208,14 +216,44 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
     for (int s = 0; s < d.k2_units; ++s) units[2].push_back({i, s});
   }
   h->w1fold_stride = w1fold_floats(h->hp, h->path);
+  // L2-sized groups: consecutive tensors whose state (p, g, m0..2, v: 24
+  // bytes per element) fits in sweep_bytes; a larger tensor is a group of
+  // its own.  The units of every kernel are in tensor order here.
+  h->groups.clear();
+  if (h->sweep_bytes > 0 && !global_rows) {
+    int64_t bytes = 0;
+    int first[3] = {0, 0, 0}, end[3] = {0, 0, 0};
+    for (int i = 0; i < n; ++i) {
+      const int64_t b = 24 * desc[i].N;
+      if (i > 0 && bytes + b > h->sweep_bytes) {
+        h->groups.push_back({{first[0], first[1], first[2]},
+                             {end[0] - first[0], end[1] - first[1], end[2] - first[2]}});
+        for (int k = 0; k < 3; ++k) first[k] = end[k];
+        bytes = 0;
+      }
+      bytes += b;
+      end[0] += desc[i].n_strips;
+      end[1] += desc[i].k1_units;
+      end[2] += desc[i].k2_units;
+    }
+    h->groups.push_back({{first[0], first[1], first[2]},
+                         {end[0] - first[0], end[1] - first[1], end[2] - first[2]}});
+  }
   // K0 blocks are dispatched about in unit order: the largest strips first
   // (whose tensors also have the longest column finalisation), so that the
-  // launch ends on small strips.  Results do not depend on this order.
-  std::stable_sort(units[0].begin(), units[0].end(), [&](const Unit& x, const Unit& y) {
+  // launch ends on small strips -- within each group when there are groups.
+  // Results do not depend on this order.
+  auto by_strip = [&](const Unit& x, const Unit& y) {
     const TensorDesc& a = desc[x.tensor];
     const TensorDesc& b = desc[y.tensor];
     return (int64_t)a.strip_rows * a.C > (int64_t)b.strip_rows * b.C;
-  });
+  };
+  if (h->groups.empty()) {
+    std::stable_sort(units[0].begin(), units[0].end(), by_strip);
+  } else {
+    for (const auto& g : h->groups)
+      std::stable_sort(units[0].begin() + g.first[0], units[0].begin() + g.first[0] + g.count[0], by_strip);
+  }
 
   // carve the workspace
   size_t off = 0;
@@ -285,6 +323,7 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
   if (global_rows) h->last_grows.assign(global_rows, global_rows + n);
   else h->last_grows.clear();
   h->last_path = h->path;
+  h->last_sweep = h->sweep_bytes;
   return LOPT_OK;
 }
 
@@ -496,6 +535,12 @@ int lopt_set_mlp_path(lopt_handle h, int path) {
   return LOPT_E_ARG;
 }
 
+int lopt_set_sweep_bytes(lopt_handle h, int64_t group_bytes) {
+  if (!h || group_bytes < 0) return LOPT_E_ARG;
+  h->sweep_bytes = group_bytes;   // a changed setting rebuilds the schedule on the next step
+  return LOPT_OK;
+}
+
 int lopt_set_weight_decay(lopt_handle h, float weight_decay) {
   if (!h || !(weight_decay >= 0.f) || !std::isfinite(weight_decay)) return LOPT_E_ARG;
   h->weight_decay = weight_decay;
@@ -510,7 +555,7 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_ptr);
 
   if (h->shard_phase != 0) return LOPT_E_ARG;   // a row-sharded step is in progress
-  const bool same = h->last_path == h->path && h->last_grows.empty() &&
+  const bool same = h->last_path == h->path && h->last_grows.empty() && h->last_sweep == h->sweep_bytes &&
                     (int)h->last_list.size() == n_tensors &&
                     std::memcmp(h->last_list.data(), tensors, sizeof(lopt_tensor) * n_tensors) == 0;
   if (!same) {
@@ -562,43 +607,55 @@ int lopt_step(lopt_handle h, const lopt_tensor* tensors, int n_tensors, int64_t 
   a.wd = h->weight_decay;
   a.status = h->d_status;
 
-  cudaEvent_t* ev = nullptr;
-  if (h->timing) {
-    if (h->tev_used + 4 > h->tev.size()) {
-      for (int k = 0; k < 4; ++k) {
-        cudaEvent_t x;
-        e = cudaEventCreate(&x);
-        if (e != cudaSuccess) return cuda_fail(e);
-        h->tev.push_back(x);
+  // One launch of each kernel over the whole list, or, with L2-sized groups,
+  // the three launches per group, group after group.
+  const int n_groups = h->groups.empty() ? 1 : (int)h->groups.size();
+  for (int gi = 0; gi < n_groups && e == cudaSuccess; ++gi) {
+    int first[3] = {0, 0, 0}, count[3] = {h->n_units[0], h->n_units[1], h->n_units[2]};
+    if (!h->groups.empty()) {
+      for (int k = 0; k < 3; ++k) {
+        first[k] = h->groups[gi].first[k];
+        count[k] = h->groups[gi].count[k];
       }
     }
-    ev = h->tev.data() + h->tev_used;
-    h->tev_used += 4;
-  }
-  auto mark = [&](int k) {
-    if (ev && e == cudaSuccess) e = cudaEventRecord(ev[k], stream);
-  };
+    cudaEvent_t* ev = nullptr;   // kernel timing: 4 events per group
+    if (h->timing) {
+      if (h->tev_used + 4 > h->tev.size()) {
+        for (int k = 0; k < 4; ++k) {
+          cudaEvent_t x;
+          e = cudaEventCreate(&x);
+          if (e != cudaSuccess) return cuda_fail(e);
+          h->tev.push_back(x);
+        }
+      }
+      ev = h->tev.data() + h->tev_used;
+      h->tev_used += 4;
+    }
+    auto mark = [&](int k) {
+      if (ev && e == cudaSuccess) e = cudaEventRecord(ev[k], stream);
+    };
 
-  mark(0);
-  a.units = h->d_units[0];
-  a.n_units = h->n_units[0];
-  a.counters = h->d_counters;
-  if (e == cudaSuccess) e = launch_rowcol(a, stream);
-  mark(1);
-  if (e == cudaSuccess) {
-    a.units = h->d_units[1];
-    a.n_units = h->n_units[1];
-    a.counters = h->d_counters + n_tensors;
-    e = launch_stats(a, stream);
+    mark(0);
+    a.units = h->d_units[0] + first[0];
+    a.n_units = count[0];
+    a.counters = h->d_counters;
+    if (e == cudaSuccess) e = launch_rowcol(a, stream);
+    mark(1);
+    if (e == cudaSuccess) {
+      a.units = h->d_units[1] + first[1];
+      a.n_units = count[1];
+      a.counters = h->d_counters + n_tensors;
+      e = launch_stats(a, stream);
+    }
+    mark(2);
+    if (e == cudaSuccess) {
+      a.units = h->d_units[2] + first[2];
+      a.n_units = count[2];
+      a.counters = nullptr;
+      e = (h->path == LOPT_MLP_TC) ? launch_apply_tc(a, stream) : launch_apply_fp32(a, stream);
+    }
+    mark(3);
   }
-  mark(2);
-  if (e == cudaSuccess) {
-    a.units = h->d_units[2];
-    a.n_units = h->n_units[2];
-    a.counters = nullptr;
-    e = (h->path == LOPT_MLP_TC) ? launch_apply_tc(a, stream) : launch_apply_fp32(a, stream);
-  }
-  mark(3);
   if (e != cudaSuccess) {
     h->last_list.clear();
     return cuda_fail(e);

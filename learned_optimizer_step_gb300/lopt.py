@@ -31,7 +31,8 @@ ERRORS = {
     -9: "LOPT_E_TOO_LARGE",
 }
 
-EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_set_weight_decay", "lopt_step",
+EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_set_weight_decay",
+            "lopt_set_sweep_bytes", "lopt_step",
             "lopt_step_host", "lopt_host_sync", "lopt_set_host_groups",
             "lopt_shard_sizes", "lopt_shard_begin", "lopt_shard_middle", "lopt_shard_end",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
@@ -76,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_set_mlp_path.restype = i32
     lib.lopt_set_weight_decay.argtypes = [vp, ctypes.c_float]
     lib.lopt_set_weight_decay.restype = i32
+    lib.lopt_set_sweep_bytes.argtypes = [vp, i64]
+    lib.lopt_set_sweep_bytes.restype = i32
     lib.lopt_step.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, i64, ctypes.c_float, vp]
     lib.lopt_step_host.restype = i32
     lib.lopt_step_host.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(vp), ctypes.POINTER(vp),
@@ -229,6 +232,12 @@ class LearnedOptimizer:
     def set_weight_decay(self, weight_decay: float) -> None:
         """Decoupled weight decay of later steps: p -= lr * (update + wd * p)."""
         _check("lopt_set_weight_decay", load_library().lopt_set_weight_decay(self._h, float(weight_decay)))
+
+    def set_sweep_bytes(self, group_bytes: int) -> None:
+        """Groups of consecutive tensors with at most ``group_bytes`` of state
+        (24 bytes per element) run the three kernels one group after the
+        other, so that re-reads come from L2; 0 turns it off."""
+        _check("lopt_set_sweep_bytes", load_library().lopt_set_sweep_bytes(self._h, int(group_bytes)))
 
     def prepare(self, tensors: Sequence) -> PreparedList:
         ts = [t if isinstance(t, TensorState) else TensorState.from_dict(t) for t in tensors]

@@ -86,6 +86,32 @@ def test_ragged_launch_equals_solo_launches_bitwise(path):
 
 
 @pytest.mark.parametrize("path", ["fp32", "tc"])
+@pytest.mark.parametrize("group_bytes", [1, 24 * 40_000, 24 * 400_000])
+def test_l2_groups_equal_one_launch_bitwise(path, group_bytes):
+    """Single sweep through L2 (lopt_set_sweep_bytes): the list run group by
+    group, from one tensor per group to a few groups, gives the same bits as
+    one launch of each kernel over the whole list."""
+    torch = need_gpu()
+    eng, w = engine(n_sets=1, path=path)
+    shapes = EDGE_SHAPES + [("big", (600, 700)), ("mid", (300, 200)), ("vec", (5000,))]
+    a = make_states(shapes, recipe="vit", seed=8)
+    b = make_states(shapes, recipe="vit", seed=8)
+    for t in (1, 2):
+        eng.set_sweep_bytes(0)
+        eng.step(a, t, 1.0)
+        eng.set_sweep_bytes(group_bytes)
+        eng.step(b, t, 1.0)
+    eng.set_sweep_bytes(0)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        for k in ("param", "rms"):
+            assert torch.equal(x[k], y[k]), x["name"]
+        for k in ("mom", "row", "col"):
+            for u, v in zip(x[k], y[k]):
+                assert torch.equal(u, v), x["name"]
+
+
+@pytest.mark.parametrize("path", ["fp32", "tc"])
 def test_two_runs_are_bitwise_identical(path):
     torch = need_gpu()
     eng, w = engine(path=path)
