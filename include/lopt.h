@@ -359,6 +359,22 @@ int lopt_rowcol_static(const float* grad, float* const* row, float* const* col,
                        int64_t rows, int64_t cols, float* inv_rho, void* stream);
 
 /* Release every device allocation of the handle (waits for its work). */
+/*
+ * Self-test of failure detection, for the current device.  Every wait of
+ * the library's kernels on an mbarrier (a pipeline stage, an MMA
+ * completion) is bounded by %globaltimer: when it runs out, the kernel
+ * raises a timeout flag that lopt_check() reports as LOPT_E_TIMEOUT, every
+ * role stops, and the CUDA context stays usable.  This call runs that same
+ * bounded wait in one block of 32 threads on a barrier that expects two
+ * arrivals and gets one, so that it must run out after limit_ns
+ * nanoseconds (1 .. 1e9), and synchronises with the device.
+ * Returns LOPT_E_TIMEOUT when the wait gave up and raised the flag, as
+ * designed; LOPT_OK would mean that the wait had returned on a phase that
+ * never completed.  Errors: LOPT_E_ARG (limit out of range), LOPT_E_OOM,
+ * LOPT_E_CUDA.
+ */
+int lopt_selftest_wait(int64_t limit_ns);
+
 int lopt_destroy(lopt_handle h);
 
 /* Static string naming an error code. */

@@ -535,6 +535,24 @@ int lopt_set_mlp_path(lopt_handle h, int path) {
   return LOPT_E_ARG;
 }
 
+int lopt_selftest_wait(int64_t limit_ns) {
+  if (limit_ns <= 0 || limit_ns > 1000000000) return LOPT_E_ARG;
+  int32_t* d_status = nullptr;
+  cudaError_t e = cudaMalloc(&d_status, sizeof(int32_t));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return LOPT_E_OOM;
+  }
+  int32_t status = 0;
+  e = cudaMemset(d_status, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = launch_wait_probe(limit_ns, d_status, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&status, d_status, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  cudaFree(d_status);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return (status & kStatusTimeout) ? LOPT_E_TIMEOUT : LOPT_OK;
+}
+
 int lopt_set_sweep_bytes(lopt_handle h, int64_t group_bytes) {
   if (!h || group_bytes < 0) return LOPT_E_ARG;
   h->sweep_bytes = group_bytes;   // a changed setting rebuilds the schedule on the next step

@@ -36,7 +36,8 @@ EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_se
             "lopt_step_host", "lopt_host_sync", "lopt_set_host_groups",
             "lopt_shard_sizes", "lopt_shard_begin", "lopt_shard_middle", "lopt_shard_end",
             "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
-            "lopt_rowcol_static", "lopt_destroy", "lopt_strerror", "lopt_last_cuda_error", "lopt_version")
+            "lopt_rowcol_static", "lopt_selftest_wait", "lopt_destroy", "lopt_strerror", "lopt_last_cuda_error",
+            "lopt_version")
 
 
 class LoptTensor(ctypes.Structure):
@@ -79,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_set_weight_decay.restype = i32
     lib.lopt_set_sweep_bytes.argtypes = [vp, i64]
     lib.lopt_set_sweep_bytes.restype = i32
+    lib.lopt_selftest_wait.argtypes = [i64]
+    lib.lopt_selftest_wait.restype = i32
     lib.lopt_step.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, i64, ctypes.c_float, vp]
     lib.lopt_step_host.restype = i32
     lib.lopt_step_host.argtypes = [vp, ctypes.POINTER(LoptTensor), i32, ctypes.POINTER(vp), ctypes.POINTER(vp),

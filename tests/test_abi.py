@@ -81,6 +81,8 @@ def test_validation_before_any_device_call(lib):
     assert lib.lopt_set_mlp_path(None, 0) == -1
     assert lib.lopt_set_weight_decay(None, 0.0) == -1
     assert lib.lopt_set_sweep_bytes(None, 0) == -1
+    assert lib.lopt_selftest_wait(0) == -1
+    assert lib.lopt_selftest_wait(2_000_000_000) == -1
     assert lib.lopt_feature_stats(None, 0, None) == -1
     assert lib.lopt_set_kernel_timing(None, 1) == -1
     assert lib.lopt_kernel_times(None, None, None) == -1
