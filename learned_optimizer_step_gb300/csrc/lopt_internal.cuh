@@ -253,8 +253,6 @@ cudaError_t launch_rowcol_finish(const StepArgs& a, int n_tensors, cudaStream_t 
 cudaError_t launch_stats_finish(const StepArgs& a, int n_tensors, cudaStream_t s);
 cudaError_t launch_apply_fp32(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_apply_tc(const StepArgs& a, cudaStream_t s);
-// One block that waits on a barrier nothing completes (bounded wait self-test).
-cudaError_t launch_wait_probe(int64_t limit_ns, int32_t* status, cudaStream_t s);
 bool apply_tc_supported(int hidden);
 int  w1fold_floats(int hidden, int path);
 size_t tc_weights_bytes(int hidden, int n_sets);
