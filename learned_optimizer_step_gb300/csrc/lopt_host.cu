@@ -24,6 +24,8 @@
 
 namespace lopt {
 bool apply_fp32_supported(int hidden);
+// k_probe.cu: one block that waits on a barrier nothing completes.
+cudaError_t launch_wait_probe(int64_t limit_ns, int32_t* status, cudaStream_t s);
 
 namespace {
 // The last CUDA error a call of this thread failed on (lopt_last_cuda_error).
@@ -534,11 +536,6 @@ int lopt_set_mlp_path(lopt_handle h, int path) {
   }
   return LOPT_E_ARG;
 }
-
-namespace lopt {
-// k_probe.cu: one block that waits on a barrier nothing completes.
-cudaError_t launch_wait_probe(int64_t limit_ns, int32_t* status, cudaStream_t s);
-}  // namespace lopt
 
 int lopt_selftest_wait(int64_t limit_ns) {
   if (limit_ns <= 0 || limit_ns > 1000000000) return LOPT_E_ARG;
