@@ -137,6 +137,17 @@ def dp_rms_err(p_old, got_new, ref_new) -> float:
     return float(np.sqrt(np.mean(e * e))) / max(float(np.sqrt(np.mean(dref * dref))), 1e-300)
 
 
+def report(test: str, path: str, worst: dict) -> None:
+    """Appends the worst errors a test measured to the JSON-lines file named
+    by LOPT_PARITY_REPORT, when that is set (for the design notes)."""
+    import json
+    import os
+    out = os.environ.get("LOPT_PARITY_REPORT")
+    if out:
+        with open(out, "a") as fh:
+            fh.write(json.dumps({"test": test, "path": path, "worst": worst}) + "\n")
+
+
 def made_of_update(p_old, ref_new) -> bool:
     p_old = np.asarray(p_old, dtype=np.float64).ravel()
     d = p_old - np.asarray(ref_new, dtype=np.float64).ravel()
@@ -182,7 +193,9 @@ def check_tensor(eng, idx, st, pre, t, lr, w, tol, sidx=None, wd=0.0, worst=None
     GPU tensor ``idx`` and applies every gate to the GPU's result; ``sidx``
     restricts the parameter comparison to sampled elements."""
     from tests import tc_emulation as E
-    worst = {"param": 0.0, "acc": 0.0, "stats": 0.0} if worst is None else worst
+    worst = {} if worst is None else worst
+    for key in ("param", "acc", "stats"):
+        worst.setdefault(key, 0.0)
     r, e = pre
     p_old = r["param"].copy()
     out = O.step_tensor(r, t, lr, w, sample_idx=sidx, weight_decay=wd)

@@ -15,7 +15,7 @@ import pytest
 import oracle as O
 import synth
 from tests import tc_emulation as E
-from tests.gpu_helpers import TOL_FP32, TOL_TC, check_param, cpu, need_gpu, rel_err, to_oracle
+from tests.gpu_helpers import TOL_FP32, TOL_TC, check_param, cpu, need_gpu, rel_err, report, to_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -84,13 +84,15 @@ def _run(workload, path, tol):
     eng.step(states, wl.first_step, 1.0)
     eng.check()
     torch.cuda.synchronize()
+    worst = {}
     for i, r in ref.items():
         st = states[i]
         got = cpu(st["param"])[r["sidx"]]
-        check_param(st["name"], tol, r["p_old"], got, r["param"], r["emu"] if tol > TOL_FP32 else None)
+        check_param(st["name"], tol, r["p_old"], got, r["param"], r["emu"] if tol > TOL_FP32 else None, worst=worst)
         assert rel_err(eng.feature_stats(i), r["S"], floor=1e-300) <= 2e-5, st["name"]
         assert rel_err(cpu(st["col"][0]), r["col0"]) <= 2e-6, st["name"]
         assert rel_err(cpu(st["mom"][1])[r["sidx"]], r["mom1_sample"]) <= 2e-6, st["name"]
+    report(workload, path, worst)
     eng.close()
     del states
     torch.cuda.empty_cache()

@@ -14,7 +14,7 @@ import pytest
 
 import oracle as O
 import synth
-from tests.gpu_helpers import (TOL_FP32, TOL_TC, check_param, check_tensor, compare_step, cpu,
+from tests.gpu_helpers import (TOL_FP32, TOL_TC, check_param, check_tensor, compare_step, cpu, report,
                                make_states, need_gpu, rel_err, snapshot, to_oracle)
 
 pytestmark = pytest.mark.gpu
@@ -268,9 +268,11 @@ def test_vit_b16_full_size_sampled(path, tol):
     torch.cuda.synchronize()
     ws = O.unpack_weights(w[0], 32)
     pick = _sample()
+    worst = {}
     for idx, st in enumerate(states):
         if id(st) in pre:
-            check_tensor(eng, idx, st, pre[id(st)], 1, 1.0, ws, tol, pick(st))
+            check_tensor(eng, idx, st, pre[id(st)], 1, 1.0, ws, tol, pick(st), worst=worst)
+    report("vit_b16", path, worst)
 
 
 @pytest.mark.parametrize("path,tol", PATHS)
@@ -288,10 +290,12 @@ def test_gpt2_heavy_tails_late_step_sampled(path, tol):
     torch.cuda.synchronize()
     ws = O.unpack_weights(w[0], 32)
     pick = _sample(seed=1)
+    worst = {}
     for idx, st in enumerate(states):
         if id(st) in pre:
             check_tensor(eng, idx, st, pre[id(st)], wl.first_step, 1.0, ws, tol, pick(st),
-                         check_acc=False)
+                         check_acc=False, worst=worst)
+    report("gpt2_small", path, worst)
 
 
 @pytest.mark.parametrize("path,tol", PATHS)
