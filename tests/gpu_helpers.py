@@ -11,8 +11,8 @@ import synth
 
 # Tolerances (reading R10, per tensor, element by element).
 #  * Updated parameters p_new: |got - ref| / max(|ref|, RMS of ref over the
-#    tensor) <= TOL_P[path]: 1e-5 on the FP32 path, 2e-3 on the tensor-core
-#    path (the benchmark spec's bounds).  On the tensor-core path the bound applies
+#    tensor) <= TOL_P[path]: 1e-5 on the FP32 path (FP32 arithmetic), 2e-3
+#    on the tensor-core path (TF32/BF16-class operands).  On the tensor-core path the bound applies
 #    to every tensor that is not made of update, i.e. whose pre-step RMS is at
 #    least ten times the RMS of its update; a zero-initialised bias after a
 #    few steps is all update and is held by the update gate alone.
