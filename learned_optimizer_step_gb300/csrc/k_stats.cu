@@ -38,6 +38,7 @@ namespace {
 
 constexpr int kT = kStatsThreads;
 constexpr int kWarps = kT / 32;
+constexpr int kFinalGroups = kT / kStats;   // threads per feature in a tensor's final sum (9)
 
 __device__ __forceinline__ void accumulate_element(const TensorDesc& d, const float inv_rho[3],
                                                    int64_t e, int64_t i, int64_t j,
@@ -77,6 +78,7 @@ __device__ void fold_first_layer(const StepArgs& a, int T, const TensorDesc& d, 
 
 __global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per SM for loads in flight
   __shared__ float red[kWarps][kStats];
+  __shared__ double fin[kFinalGroups][kStats];
   __shared__ double scale[kStats];
   __shared__ int is_last;
 
@@ -168,11 +170,23 @@ __global__ void __launch_bounds__(kT, 3) k_stats(StepArgs a) {   // 3 blocks per
   if (!is_last) return;
   __threadfence();
 
-  // ---- finalize this tensor: S_d in unit order, in double -----------------
-  if (tid < kStats) {
+  // ---- finalize this tensor: S_d in double, in a fixed order -------------
+  // kFinalGroups threads per feature each add, in increasing order, the
+  // partials of the units x = g mod kFinalGroups; then their sums are added
+  // in g order.  (One thread per feature adding thousands of partials in
+  // turn was the tail of the launch for the largest tensors.)
+  if (tid < kFinalGroups * kStats) {
+    const int f = tid % kStats, g = tid / kStats;
     const float* part = a.k1part + d.k1_part_off;
     double s = 0.0;
-    for (int x = 0; x < d.k1_units; ++x) s += (double)__ldcg(part + (int64_t)x * kStats + tid);
+    for (int x = g; x < d.k1_units; x += kFinalGroups) s += (double)__ldcg(part + (int64_t)x * kStats + f);
+    fin[g][f] = s;
+  }
+  __syncthreads();
+  if (tid < kStats) {
+    double s = 0.0;
+#pragma unroll
+    for (int g = 0; g < kFinalGroups; ++g) s += fin[g][tid];
     if (a.xch2) {   // row-sharded: this rank's sums go out for the exchange
       a.xch2[(int64_t)u.tensor * kStats + tid] = s;
     } else {

@@ -40,11 +40,19 @@ int record_cuda_error(cudaError_t e) {
 
 // Rows per K0 strip.  About kStripTarget elements per strip, but no more
 // than kFinalizeCap / cols strips (the last block of a tensor sums
-// strips x cols column partials) and no more than kMaxStripRows rows.
+// strips x cols column partials) -- unless strips would then exceed
+// kMaxStripElems elements, since a very large tensor in a few huge strips
+// leaves the launch waiting on a few blocks; then up to 4 x kFinalizeCap
+// partials (1 MB, inside the no-allocation scratch) -- and no more than
+// kMaxStripRows rows.
+constexpr int64_t kMaxStripElems = 131072;
 int strip_rows_for(int64_t R, int64_t C) {
   const int64_t N = R * C;
+  const int64_t Cc = std::max<int64_t>(C, 1);
   int64_t strips = std::max<int64_t>(1, (N + kStripTarget - 1) / kStripTarget);
-  strips = std::min<int64_t>(strips, std::max<int64_t>(1, kFinalizeCap / std::max<int64_t>(C, 1)));
+  const int64_t cap = std::max<int64_t>(kFinalizeCap / Cc,
+                                        std::min<int64_t>((N + kMaxStripElems - 1) / kMaxStripElems, 4 * kFinalizeCap / Cc));
+  strips = std::min<int64_t>(strips, std::max<int64_t>(1, cap));
   strips = std::min<int64_t>(strips, R);
   int64_t rows = (R + strips - 1) / strips;
   rows = std::min<int64_t>(rows, kMaxStripRows);
@@ -250,11 +258,18 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
     const TensorDesc& b = desc[y.tensor];
     return (int64_t)a.strip_rows * a.C > (int64_t)b.strip_rows * b.C;
   };
+  // K1 blocks likewise take the largest tensors first: the last block of a
+  // tensor sums its partials, and a large tensor's sum at the end of the
+  // launch would be its tail.
+  auto by_size = [&](const Unit& x, const Unit& y) { return desc[x.tensor].N > desc[y.tensor].N; };
   if (h->groups.empty()) {
     std::stable_sort(units[0].begin(), units[0].end(), by_strip);
+    std::stable_sort(units[1].begin(), units[1].end(), by_size);
   } else {
-    for (const auto& g : h->groups)
+    for (const auto& g : h->groups) {
       std::stable_sort(units[0].begin() + g.first[0], units[0].begin() + g.first[0] + g.count[0], by_strip);
+      std::stable_sort(units[1].begin() + g.first[1], units[1].begin() + g.first[1] + g.count[1], by_size);
+    }
   }
 
   // carve the workspace
