@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--workload", default="vit_b16")
     ap.add_argument("--mlp", default="auto", choices=["auto", "tc", "fp32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--host-groups", type=int, default=0,
+                    help="most groups of tensors per host-buffer step (0: the library's default)")
     ap.add_argument("--profile-one-step", action="store_true",
                     help="after the warm-up, one extra step between cudaProfilerStart and cudaProfilerStop "
                          "(for ncu --profile-from-start off)")
@@ -388,6 +390,8 @@ def run_ours(args, rank, world, local_rank):
             path = "fp32"
     if args.sweep_mb > 0:
         eng.set_sweep_bytes(int(args.sweep_mb * 2 ** 20))
+    if args.host_groups > 0:
+        eng.set_host_groups(args.host_groups)
     prepared = eng.prepare(states)
     numel = prepared.numel
     stream = torch.cuda.current_stream()
