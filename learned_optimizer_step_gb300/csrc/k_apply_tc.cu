@@ -46,7 +46,9 @@
 // measured to slow the kernel: their polling takes issue slots from the
 // feature warps.)  At most S tiles are in flight (10 slots at NP = 32), and
 // a tile keeps its slot from its features to the read of its layer-2
-// result, so S tiles per slot lifetime bound the throughput; hence the
+// result (its release is a barrier per tile in rotation, so that no wait
+// can mistake an older release of the same slot for it), so S tiles per
+// slot lifetime bound the throughput; hence the
 // epilogue's lag of two pairs between layer 1 and the rest of a pair (by
 // then layer 2 has usually completed), and no third MMA for the output
 // layer: its round trip lengthens the lifetime more than it shortens the
@@ -93,6 +95,14 @@ constexpr int kLag = 2;
 // the MMA threads can get no further ahead than the stages the other
 // epilogue groups own plus one slot round: fewer than kEpiGroups *
 // kStageTiles + S tiles, well under kDone pairs.
+// Slot releases likewise have one barrier per tile in rotation, not one
+// per slot: a waiter for the release of tile k - S (waited for by parity)
+// must find the release of tile k - S - kDone complete, which a per-slot
+// barrier (kDone = S) would not guarantee -- that earlier release may come
+// from the other epilogue group, arbitrarily late.  Tile k - S - kDone lies
+// in a stage at least kRingStages before tile k's, and such a stage is done
+// before tile k's stage is loaded; and tile k - S + kDone cannot be
+// released before tile k is handed over.
 constexpr int kDone = 64;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -143,7 +153,7 @@ struct Geom {
   static constexpr int oB1 = oRing + kRingStages * kStageBytes;
   static constexpr int oB2 = oB1 + B1;                  // B2, b2, W3, b3 as packed
   static constexpr int oBar = (oB2 + Set + 15) / 16 * 16;
-  static constexpr int nBars = 2 * kRingStages + 3 * S + 2 * kDone;
+  static constexpr int nBars = 2 * kRingStages + 2 * S + 3 * kDone;
   static constexpr int oRec = (oBar + nBars * 8 + 15) / 16 * 16;   // records are read as float4
   static constexpr int oInfo = oRec + kRingStages * (int)sizeof(StageRec);
   static constexpr int Smem = oInfo + 64;
@@ -155,6 +165,8 @@ struct Geom {
   static_assert(S % 2 == 0, "tile pairs start on even slots");
   static_assert(S * SlotCols <= 512 && S > kStageTiles && kDone >= kEpiGroups * kStageTiles + S,
                 "tensor memory columns / pipeline depth");
+  static_assert(S + kDone > kRingStages * kStageTiles && kDone - S >= kRingStages * kStageTiles,
+                "slot releases are never waited for a round behind nor lapped");
   static_assert(oRec % 16 == 0 && sizeof(StageRec) % 16 == 0, "16-byte aligned stage records");
 };
 
@@ -406,8 +418,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
   uint64_t* stage_done = ring_full + R;
   uint64_t* a1_full = stage_done + R;
   uint64_t* a2_full = a1_full + S;
-  uint64_t* slot_empty = a2_full + S;
-  uint64_t* done1 = slot_empty + S;
+  uint64_t* freed = a2_full + S;       // per tile in rotation: its slot is free again
+  uint64_t* done1 = freed + kDone;
   uint64_t* done2 = done1 + kDone;
   StageRec* rec = reinterpret_cast<StageRec*>(smem + G::oRec);
   int32_t* info = reinterpret_cast<int32_t*>(smem + G::oInfo);   // session: end unit, tiles
@@ -445,8 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
       for (int s = 0; s < S; ++s) {
         mbar_init(a1_full + s, kTile);
         mbar_init(a2_full + s, kTile);
-        mbar_init(slot_empty + s, kTile);
+
       }
+      for (int x = 0; x < kDone; ++x) mbar_init(freed + x, kTile);
       for (int s = 0; s < 2 * kDone; ++s) mbar_init(done1 + s, 1);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -619,19 +632,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           float* const sbase = ring + si.st * (kArrays * kStageElems);
           const int nq = stage_tiles(si.n) / 4;
           int s = si.k0 % S;                          // slot of the stage's first tile
-          uint32_t sph = (uint32_t)((si.k0 / S) & 1);  // its round parity
+          // The next tile, k, may use its slot once tile k - S has released
+          // it.  Releases have a barrier per tile in rotation (kDone), so that
+          // a release that is waited for by parity cannot be confused with a
+          // late release of an earlier tile of the same slot.  fj, fph: the
+          // rotation index and phase parity of tile k - S (floor semantics:
+          // for the first S tiles of a session, parity 1 of a fresh barrier,
+          // which passes at once).
+          int fj = (si.k0 - S) & (kDone - 1);
+          uint32_t fph = (uint32_t)((si.k0 - S) >> 6) & 1u;
+          static_assert(kDone == 64, "rotation parity by shift");
           // Hands a tile's A operand to its slot and tells the layer-1 MMA
           // thread at once.  The slot is waited for only now, so that loads
           // and arithmetic overlap the wait.  (Announcing a tile only at the
           // next tile, to avoid waiting for the store, was measured to delay
           // the layer-1 MMA by about 450 cycles.)
           auto emit = [&](const uint32_t (&av)[16]) -> bool {
-            if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag)) return false;
+            if (!mbar_wait_or_abort(freed + fj, fph, kWaitNs, abort_flag)) return false;
             tmem_st16(t_lane + s * G::SlotCols + NP, av);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(a1_full + s);
-            if (++s == S) { s = 0; sph ^= 1u; }
+            if (++s == S) s = 0;
+            if (++fj == kDone) { fj = 0; fph ^= 1u; }
             return true;
           };
           // The same for two tiles at once (one wait for both stores), in two
@@ -640,9 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
           // both tiles announced.
           auto store_lo_pair = [&](const uint32_t (&loA)[8], const uint32_t (&loB)[8]) -> bool {
             const int s1 = s + 1 == S ? 0 : s + 1;
-            const uint32_t ph1 = s1 == 0 ? sph ^ 1u : sph;
-            if (!mbar_wait_or_abort(slot_empty + s, sph ^ 1u, kWaitNs, abort_flag) ||
-                !mbar_wait_or_abort(slot_empty + s1, ph1 ^ 1u, kWaitNs, abort_flag))
+            const int fj1 = fj + 1 == kDone ? 0 : fj + 1;
+            const uint32_t fph1 = fj1 == 0 ? fph ^ 1u : fph;
+            if (!mbar_wait_or_abort(freed + fj, fph, kWaitNs, abort_flag) ||
+                !mbar_wait_or_abort(freed + fj1, fph1, kWaitNs, abort_flag))
               return false;
             tmem_st8(t_lane + s * G::SlotCols + NP, loA);
             tmem_st8(t_lane + s1 * G::SlotCols + NP, loB);
@@ -657,7 +681,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
             mbar_arrive(a1_full + s);
             mbar_arrive(a1_full + s1);
             s = s1 + 1 == S ? 0 : s1 + 1;
-            if (s1 == 0 || s == 0) sph ^= 1u;   // passed the end of the ring
+            const int fj1 = fj + 1 == kDone ? 0 : fj + 1;
+            fj = fj1 + 1 == kDone ? 0 : fj1 + 1;
+            if (fj1 == 0 || fj == 0) fph ^= 1u;   // passed the end of the rotation
           };
           for (int qd = 0; ok && qd < nq; ++qd) {
             const int x0 = qd * kQuadElems + 4 * t;   // this lane's first element in the stage
@@ -846,8 +872,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_apply_tc(StepArgs a) {
               tmem_wait_ld();
               if (hf == NP / 16 - 1) {
                 tc_fence_before();
-                mbar_arrive(slot_empty + s);
-                mbar_arrive(slot_empty + s1);
+                mbar_arrive(freed + (k & (kDone - 1)));
+                mbar_arrive(freed + ((k + 1) & (kDone - 1)));
               }
 #pragma unroll
               for (int ch = 0; ch < 2; ++ch) {   // 8 hidden units
