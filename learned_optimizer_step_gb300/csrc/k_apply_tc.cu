@@ -281,7 +281,7 @@ __device__ __forceinline__ void row_terms_f16(const float (&r)[3], const float (
 // features themselves, which go to FP16, use paired FP32 multiplies where two
 // neighbouring features share the operation, and a fused multiply-add
 // inside rsqrt(r c / rho + eps).  rr, sr: the element's row terms.
-__device__ __forceinline__ void features_f16(float p, float g, float (&m)[3], float& v, const float (&rr)[3],
+__device__ __noinline__ void features_f16(float p, float g, float (&m)[3], float& v, const float (&rr)[3],
                                              const float (&sr)[3], const float (&c)[3], const float* sc,
                                              uint32_t (&av)[16]) {
 #pragma unroll

@@ -275,10 +275,10 @@ __device__ __forceinline__ void bulk_wait_all() {
 }
 
 // Wait for phase `parity` of `bar`, at most `limit_ns`; gives up early when
-// *abort becomes non-zero.  On its own timeout it sets *abort.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                                   volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// *abort becomes non-zero.  On its own timeout it sets *abort.  The polling
+// loop is out of line: it is entered only when the phase is not complete at
+// the first test, and kept out of the callers it leaves their code compact.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns, volatile int* abort) {
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < (1u << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -292,6 +292,10 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
   }
   *abort = 1;
   return false;
+}
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                                   volatile int* abort) {
+  return mbar_try_wait(bar, parity) || mbar_wait_slow(bar, parity, limit_ns, abort);
 }
 
 // Layer-1 B operand [NP x 32] (FP16) for the tensor-core path:
