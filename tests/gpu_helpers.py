@@ -51,7 +51,9 @@ TOL_TC_DP, TOL_TC_EMU, TOL_TC_DP_RMS, TOL_TC_EMU_RMS = _tc_bounds()
 MADE_OF_UPDATE = 10.0   # RMS(p_old) / RMS(dp) below which a tensor is all update
 # The RMS gates hold tensors (or samples) of at least this many elements: an
 # RMS over fewer is dominated by single elements, which the per-element gates
-# hold (the RMS bounds are measured on tensors of 768 elements and more).
+# hold (the RMS bounds are measured on whole tensors of 768 elements and more
+# and on samples of 256 elements plus the two ends, as the full-size tests
+# draw them).
 RMS_MIN_ELEMENTS = 256
 
 
