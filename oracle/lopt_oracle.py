@@ -50,10 +50,11 @@ Precision: float64 throughout (inputs arrive as float32 and are widened
 exactly).  Big tensors are processed in element chunks only to bound host
 memory; the sums over chunks are plain sums.
 
-"parity unpinned": the composition of the full MLP with random (untrained)
-weights has no published value to pin against; every stage is pinned
-separately by closed forms, invariants and brute force in
-``tests/test_oracle_pins.py``.
+Pins (``tests/test_oracle_pins.py``): the page prints no worked example, and
+the composition of the MLP with random (untrained) weights has no published
+value.  Every stage is pinned by closed forms and invariants, and the whole
+step, random weights with nonzero biases included, by an independent scalar
+brute force on tiny tensors over three steps.
 """
 
 from __future__ import annotations
