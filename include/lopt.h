@@ -288,6 +288,38 @@ int lopt_shard_middle(lopt_handle h, void* stream);
 int lopt_shard_end(lopt_handle h, void* stream);
 
 /*
+ * The launch schedule that lopt_step() builds for a tensor list, computed on
+ * the host alone (no device call, no handle; thread-safe).  The step's work
+ * is split into units ("PyLO: Towards Accessible Learned Optimizers in
+ * PyTorch", section "融合カーネル戦略": statistics over every element of a
+ * tensor before its apply pass):
+ *   K0  row strips of a tensor (row/column second moments; its last strip
+ *       sums the strips' column partials);
+ *   K1  chunks of 16,384 elements (feature square sums);
+ *   K2  chunks of 4,096 elements (normalise, MLP, update).
+ *   tensors, n_tensors  as for lopt_step(); only rows, cols, reserved and
+ *               the 16-byte alignment of the pointers are read (the
+ *               pointers are never dereferenced).
+ *   sweep_bytes as lopt_set_sweep_bytes() (0: one launch per kernel).
+ *   n_units     out, 3 ints: the units of K0, K1, K2.
+ *   units       out or NULL: 2 ints per unit, (tensor index, index of the
+ *               unit within its tensor), K0's units in launch order, then
+ *               K1's, then K2's.
+ *   strip_rows  out or NULL: n_tensors ints, the rows of each K0 strip (the
+ *               last strip of a tensor may have fewer).
+ *   n_groups    out: the groups of the single sweep (0 when sweep_bytes is 0).
+ *   groups      out or NULL: 6 ints per group: the first unit and the unit
+ *               count of K0, K1 and K2.
+ * Call with NULL units / strip_rows / groups for the counts, then again
+ * with arrays of that size.  Errors: LOPT_E_ARG (n_tensors < 0, NULL
+ * tensors with n_tensors > 0, NULL n_units or n_groups, a negative
+ * sweep_bytes, reserved != 0); LOPT_E_SHAPE (lopt_step()'s shape rules).
+ */
+int lopt_schedule_info(const lopt_tensor* tensors, int n_tensors, int64_t sweep_bytes,
+                       int32_t* n_units, int32_t* units, int32_t* strip_rows,
+                       int32_t* n_groups, int32_t* groups);
+
+/*
  * Wait for the handle's last step and report device-side status:
  * LOPT_OK, LOPT_E_TIMEOUT (a bounded wait inside a kernel gave up; that
  * step's results are invalid) or LOPT_E_CUDA.  Clears the status.

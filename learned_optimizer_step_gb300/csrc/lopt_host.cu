@@ -182,10 +182,20 @@ int validate(const lopt_ctx* h, const lopt_tensor* ts, int n, const int64_t* glo
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15) == 0; }
 
-int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t stream,
-                   const int64_t* global_rows = nullptr) {
-  std::vector<TensorDesc> desc(n);
+// The host half of a schedule: one descriptor per tensor, the unit table of
+// each kernel in launch order, the L2-sized groups, and the sizes of the
+// partial-sum areas.  No device call; the pointers are not dereferenced.
+struct Plan {
+  std::vector<TensorDesc> desc;
   std::vector<Unit> units[3];
+  std::vector<lopt_ctx::Group> groups;
+  int64_t colpart = 0, rowpart = 0, k1part = 0;
+};
+
+int plan_schedule(const lopt_tensor* ts, int n, int64_t sweep_bytes, const int64_t* global_rows, Plan& pl) {
+  std::vector<TensorDesc>& desc = pl.desc;
+  std::vector<Unit>* units = pl.units;
+  desc.assign(n, TensorDesc{});
   int64_t colpart = 0, rowpart = 0, k1part = 0, x1 = 0;
   for (int i = 0; i < n; ++i) {
     const lopt_tensor& t = ts[i];
@@ -225,19 +235,22 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
     for (int s = 0; s < d.k1_units; ++s) units[1].push_back({i, s});
     for (int s = 0; s < d.k2_units; ++s) units[2].push_back({i, s});
   }
-  h->w1fold_stride = w1fold_floats(h->hp, h->path);
+  pl.colpart = colpart;
+  pl.rowpart = rowpart;
+  pl.k1part = k1part;
   // L2-sized groups: consecutive tensors whose state (p, g, m0..2, v: 24
   // bytes per element) fits in sweep_bytes; a larger tensor is a group of
   // its own.  The units of every kernel are in tensor order here.
-  h->groups.clear();
-  if (h->sweep_bytes > 0 && !global_rows) {
+  std::vector<lopt_ctx::Group>& groups = pl.groups;
+  groups.clear();
+  if (sweep_bytes > 0 && !global_rows) {
     int64_t bytes = 0;
     int first[3] = {0, 0, 0}, end[3] = {0, 0, 0};
     for (int i = 0; i < n; ++i) {
       const int64_t b = 24 * desc[i].N;
-      if (i > 0 && bytes + b > h->sweep_bytes) {
-        h->groups.push_back({{first[0], first[1], first[2]},
-                             {end[0] - first[0], end[1] - first[1], end[2] - first[2]}});
+      if (i > 0 && bytes + b > sweep_bytes) {
+        groups.push_back({{first[0], first[1], first[2]},
+                          {end[0] - first[0], end[1] - first[1], end[2] - first[2]}});
         for (int k = 0; k < 3; ++k) first[k] = end[k];
         bytes = 0;
       }
@@ -246,8 +259,8 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
       end[1] += desc[i].k1_units;
       end[2] += desc[i].k2_units;
     }
-    h->groups.push_back({{first[0], first[1], first[2]},
-                         {end[0] - first[0], end[1] - first[1], end[2] - first[2]}});
+    groups.push_back({{first[0], first[1], first[2]},
+                      {end[0] - first[0], end[1] - first[1], end[2] - first[2]}});
   }
   // K0 blocks are dispatched about in unit order: the largest strips first
   // (whose tensors also have the longest column finalisation), so that the
@@ -262,15 +275,28 @@ int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t strea
   // tensor sums its partials, and a large tensor's sum at the end of the
   // launch would be its tail.
   auto by_size = [&](const Unit& x, const Unit& y) { return desc[x.tensor].N > desc[y.tensor].N; };
-  if (h->groups.empty()) {
+  if (groups.empty()) {
     std::stable_sort(units[0].begin(), units[0].end(), by_strip);
     std::stable_sort(units[1].begin(), units[1].end(), by_size);
   } else {
-    for (const auto& g : h->groups) {
+    for (const auto& g : groups) {
       std::stable_sort(units[0].begin() + g.first[0], units[0].begin() + g.first[0] + g.count[0], by_strip);
       std::stable_sort(units[1].begin() + g.first[1], units[1].begin() + g.first[1] + g.count[1], by_size);
     }
   }
+  return LOPT_OK;
+}
+
+int build_schedule(lopt_ctx* h, const lopt_tensor* ts, int n, cudaStream_t stream,
+                   const int64_t* global_rows = nullptr) {
+  Plan pl;
+  const int prc = plan_schedule(ts, n, h->sweep_bytes, global_rows, pl);
+  if (prc != LOPT_OK) return prc;
+  const std::vector<TensorDesc>& desc = pl.desc;
+  const std::vector<Unit>* units = pl.units;
+  const int64_t colpart = pl.colpart, rowpart = pl.rowpart, k1part = pl.k1part;
+  h->w1fold_stride = w1fold_floats(h->hp, h->path);
+  h->groups = pl.groups;
 
   // carve the workspace
   size_t off = 0;
@@ -880,6 +906,50 @@ int lopt_host_sync(lopt_handle h, void* stream_ptr) {
 int lopt_shard_sizes(const lopt_tensor* tensors, int n_tensors, int64_t* n_x1, int64_t* n_x2) {
   if (n_tensors < 0 || (n_tensors > 0 && !tensors) || !n_x1 || !n_x2) return LOPT_E_ARG;
   shard_counts(tensors, n_tensors, n_x1, n_x2);
+  return LOPT_OK;
+}
+
+int lopt_schedule_info(const lopt_tensor* tensors, int n_tensors, int64_t sweep_bytes,
+                       int32_t* n_units, int32_t* units, int32_t* strip_rows,
+                       int32_t* n_groups, int32_t* groups) {
+  if (n_tensors < 0 || (n_tensors > 0 && !tensors) || !n_units || !n_groups || sweep_bytes < 0)
+    return LOPT_E_ARG;
+  for (int i = 0; i < n_tensors; ++i) {   // lopt_step's shape rules
+    const lopt_tensor& t = tensors[i];
+    if (t.reserved != 0) return LOPT_E_ARG;
+    if (t.rows < 1 || t.cols < 1) return LOPT_E_SHAPE;
+    if (t.rows > (int64_t)1 << 31 || t.cols > (int64_t)1 << 31) return LOPT_E_SHAPE;
+    if (t.rows * t.cols >= ((int64_t)1 << 31)) return LOPT_E_SHAPE;
+  }
+  Plan pl;
+  try {
+    const int rc = plan_schedule(tensors, n_tensors, sweep_bytes, nullptr, pl);
+    if (rc != LOPT_OK) return rc;
+  } catch (const std::bad_alloc&) {
+    return LOPT_E_OOM;
+  }
+  for (int k = 0; k < 3; ++k) {
+    if (pl.units[k].size() > (size_t)INT32_MAX) return LOPT_E_SHAPE;
+    n_units[k] = (int32_t)pl.units[k].size();
+  }
+  if (units) {
+    int64_t o = 0;
+    for (int k = 0; k < 3; ++k)
+      for (const Unit& u : pl.units[k]) {
+        units[2 * o] = u.tensor;
+        units[2 * o + 1] = u.local;
+        ++o;
+      }
+  }
+  if (strip_rows)
+    for (int i = 0; i < n_tensors; ++i) strip_rows[i] = pl.desc[i].strip_rows;
+  *n_groups = (int32_t)pl.groups.size();
+  if (groups)
+    for (size_t gi = 0; gi < pl.groups.size(); ++gi)
+      for (int k = 0; k < 3; ++k) {
+        groups[6 * gi + 2 * k] = pl.groups[gi].first[k];
+        groups[6 * gi + 2 * k + 1] = pl.groups[gi].count[k];
+      }
   return LOPT_OK;
 }
 

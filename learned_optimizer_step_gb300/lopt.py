@@ -35,7 +35,7 @@ EXPORTED = ("lopt_weight_set_size", "lopt_create", "lopt_set_mlp_path", "lopt_se
             "lopt_set_sweep_bytes", "lopt_step",
             "lopt_step_host", "lopt_host_sync", "lopt_set_host_groups",
             "lopt_shard_sizes", "lopt_shard_begin", "lopt_shard_middle", "lopt_shard_end",
-            "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
+            "lopt_schedule_info", "lopt_check", "lopt_feature_stats", "lopt_set_kernel_timing", "lopt_kernel_times",
             "lopt_rowcol_static", "lopt_selftest_wait", "lopt_destroy", "lopt_strerror", "lopt_last_cuda_error",
             "lopt_version")
 
@@ -96,6 +96,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_shard_begin.argtypes = [vp, ctypes.POINTER(LoptTensor), ctypes.POINTER(i64), i32, i64, ctypes.c_float,
                                      vp, vp, vp]
     lib.lopt_shard_begin.restype = i32
+    p32 = ctypes.POINTER(ctypes.c_int32)
+    lib.lopt_schedule_info.argtypes = [ctypes.POINTER(LoptTensor), i32, i64, p32, p32, p32, p32, p32]
+    lib.lopt_schedule_info.restype = i32
     lib.lopt_shard_middle.argtypes = [vp, vp]
     lib.lopt_shard_middle.restype = i32
     lib.lopt_shard_end.argtypes = [vp, vp]
@@ -120,6 +123,35 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lopt_version.restype = i32
     _lib = lib
     return lib
+
+
+def schedule_info(shapes, sweep_bytes: int = 0) -> dict:
+    """The launch schedule lopt_step builds for tensors of these [rows x
+    cols] views (host only, no device): per kernel (K0 row strips, K1 and
+    K2 element chunks) the units in launch order as [n x 2] int32 arrays of
+    (tensor, index within the tensor); the rows of each tensor's K0 strips;
+    and the single-sweep groups as [g x 6] (first unit and count of K0, K1,
+    K2)."""
+    import numpy as np
+    lib = load_library()
+    n = len(shapes)
+    arr = (LoptTensor * max(n, 1))()
+    for i, (r, c) in enumerate(shapes):
+        arr[i].rows, arr[i].cols = int(r), int(c)
+    n_units = (ctypes.c_int32 * 3)()
+    n_groups = ctypes.c_int32()
+    _check("lopt_schedule_info", lib.lopt_schedule_info(arr, n, int(sweep_bytes), n_units, None, None,
+                                                        ctypes.byref(n_groups), None))
+    counts = [int(x) for x in n_units]
+    units = np.zeros((sum(counts), 2), dtype=np.int32)
+    strips = np.zeros(max(n, 1), dtype=np.int32)
+    groups = np.zeros((max(n_groups.value, 1), 6), dtype=np.int32)
+    as_p32 = lambda a: a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+    _check("lopt_schedule_info", lib.lopt_schedule_info(arr, n, int(sweep_bytes), n_units, as_p32(units),
+                                                        as_p32(strips), ctypes.byref(n_groups), as_p32(groups)))
+    a, b = counts[0], counts[0] + counts[1]
+    return {"k0": units[:a], "k1": units[a:b], "k2": units[b:], "strip_rows": strips[:n],
+            "groups": groups[:n_groups.value]}
 
 
 def _check(fn: str, code: int) -> None:

@@ -87,6 +87,14 @@ def test_validation_before_any_device_call(lib):
     assert lib.lopt_set_kernel_timing(None, 1) == -1
     assert lib.lopt_kernel_times(None, None, None) == -1
     assert lib.lopt_rowcol_static(None, None, None, 4, 4, None, None) == -1
+    n_units = (ctypes.c_int32 * 3)()
+    n_groups = ctypes.c_int32()
+    assert lib.lopt_schedule_info(None, 1, 0, n_units, None, None, ctypes.byref(n_groups), None) == -1
+    assert lib.lopt_schedule_info(None, 0, 0, None, None, None, ctypes.byref(n_groups), None) == -1
+    assert lib.lopt_schedule_info(None, 0, -1, n_units, None, None, ctypes.byref(n_groups), None) == -1
+    bad = (L.LoptTensor * 1)()
+    bad[0].rows, bad[0].cols, bad[0].reserved = 4, 4, 1
+    assert lib.lopt_schedule_info(bad, 1, 0, n_units, None, None, ctypes.byref(n_groups), None) == -1
 
 
 def test_binding_rejects_non_cuda_tensors():
