@@ -331,16 +331,18 @@ def traffic_per_launch(kernel_file: str, elements: int):
 
 def algorithmic_bytes(states):
     """Bytes one launch of each kernel must move: K0 reads g; K1 reads p, g,
-    m0..2, v; K2 reads them again and writes p, m0..2, v.  Rank-1 tensors
-    ([1 x n]) also read their per-element column accumulators (3 words) in
-    K1 and K2."""
+    m0..2, v; K2 reads them again and writes p, m0..2, v.  A rank-1 tensor
+    ([1 x n]) holds its column accumulators c0..2 per element: K0 reads and
+    writes them, K1 and K2 read them.  The row and column accumulators of a
+    2-D tensor (R + C words each, about 0.1 % of the bytes of the ViT-B/16
+    list) are left out."""
     k0 = k1 = k2 = 0
     for s in states:
         n = s["rows"] * s["cols"]
-        extra = 12 * n if s["rows"] == 1 else 0
-        k0 += 4 * n
-        k1 += 24 * n + extra
-        k2 += 44 * n + extra
+        cols_per_elem = s["rows"] == 1
+        k0 += 4 * n + (24 * n if cols_per_elem else 0)
+        k1 += 24 * n + (12 * n if cols_per_elem else 0)
+        k2 += 44 * n + (12 * n if cols_per_elem else 0)
     return k0, k1, k2
 
 

@@ -27,3 +27,22 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert "workload" in d["config"]
+
+
+def test_algorithmic_bytes_of_the_vit_b16_list():
+    """72 B per element of a 2-D tensor (K0 reads g; K1 reads p, g, m0..2, v;
+    K2 reads them again and writes p, m0..2, v), 120 B per element of a
+    [1 x n] view (its per-element column accumulators read and written in
+    K0, read in K1 and K2): 6.23 GB per step of the ViT-B/16 list, 0.917 ms
+    at 6,795 GB/s."""
+    sys.path.insert(0, ROOT)
+    import bench
+    import synth
+    states = [dict(zip(("rows", "cols"), synth.rows_cols(s))) for _, s in synth.vit_b16_shapes()]
+    k0, k1, k2 = bench.algorithmic_bytes(states)
+    n2 = sum(s["rows"] * s["cols"] for s in states if s["rows"] > 1)
+    n1 = sum(s["cols"] for s in states if s["rows"] == 1)
+    assert n1 + n2 == 86_415_592
+    assert k2 == 44 * n2 + 56 * n1
+    assert k0 + k1 + k2 == 72 * n2 + 120 * n1 == 6_227_832_000
+    assert abs((k0 + k1 + k2) / 6795.1e9 * 1e3 - 0.9165) < 1e-4
