@@ -346,6 +346,18 @@ def algorithmic_bytes(states):
     return k0, k1, k2
 
 
+def step_floor_bytes(states):
+    """The step's dependency-forced bytes: 72 per element of a 2-D tensor
+    (g read once for the row/column moments; p, g, m0..2, v read twice, once
+    for the statistics and once for the apply pass; p, m0..2, v written
+    once) and 104 per element of a [1 x n] view, whose per-element column
+    accumulators are read twice and written once as well (no separate
+    row/column pass is forced there).  The kernels here move 120 for such a
+    view: the row/column pass reads g and the column accumulators and writes
+    them."""
+    return sum((104 if s["rows"] == 1 else 72) * s["rows"] * s["cols"] for s in states)
+
+
 def max_over_ranks(ms: float, world: int, device) -> float:
     """The slowest rank's time: every rank's timed region ends with a barrier,
     so the job's time is the maximum."""
@@ -509,7 +521,7 @@ def run_ours(args, rank, world, local_rank):
     # the traffic record was captured with one launch per kernel
     tr = traffic_per_launch(files[dom], numel) if args.sweep_mb <= 0 else None
     roof["traffic"] = tr
-    step_bytes = sum(k_bytes)
+    step_bytes = step_floor_bytes(states)
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

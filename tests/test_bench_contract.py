@@ -30,11 +30,12 @@ def test_reference_arm_json_line():
 
 
 def test_algorithmic_bytes_of_the_vit_b16_list():
-    """72 B per element of a 2-D tensor (K0 reads g; K1 reads p, g, m0..2, v;
-    K2 reads them again and writes p, m0..2, v), 120 B per element of a
-    [1 x n] view (its per-element column accumulators read and written in
-    K0, read in K1 and K2): 6.23 GB per step of the ViT-B/16 list, 0.917 ms
-    at 6,795 GB/s."""
+    """Per kernel: K0 reads g (4 B per element), K1 reads p, g, m0..2, v
+    (24 B), K2 reads them again and writes p, m0..2, v (44 B); a [1 x n]
+    view's per-element column accumulators add 24 B to K0 (read, write) and
+    12 B to K1 and K2 (read).  The step's dependency-forced floor is 72 B
+    per element of a 2-D tensor and 104 B of a [1 x n] view: 6.23 GB per
+    step of the ViT-B/16 list, 0.916 ms at 6,795 GB/s."""
     sys.path.insert(0, ROOT)
     import bench
     import synth
@@ -43,6 +44,7 @@ def test_algorithmic_bytes_of_the_vit_b16_list():
     n2 = sum(s["rows"] * s["cols"] for s in states if s["rows"] > 1)
     n1 = sum(s["cols"] for s in states if s["rows"] == 1)
     assert n1 + n2 == 86_415_592
-    assert k2 == 44 * n2 + 56 * n1
-    assert k0 + k1 + k2 == 72 * n2 + 120 * n1 == 6_227_832_000
-    assert abs((k0 + k1 + k2) / 6795.1e9 * 1e3 - 0.9165) < 1e-4
+    assert (k0, k1, k2) == (4 * n2 + 28 * n1, 24 * n2 + 36 * n1, 44 * n2 + 56 * n1)
+    floor = bench.step_floor_bytes(states)
+    assert floor == 72 * n2 + 104 * n1 == 6_225_862_208
+    assert abs(floor / 6795.1e9 * 1e3 - 0.9162) < 1e-4
